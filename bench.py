@@ -1,0 +1,438 @@
+#!/usr/bin/env python
+"""Benchmark of the candidate-set scoring head on GB300.
+
+One step = one pass of the whole path over one batch: for the default workload
+(256 binary questions, d=2560, V=248320) that is the full-vocabulary pass
+(pre-pass, tcgen05 head, split merge, set rules) followed by the restricted
+26-code pass (pre-pass, restricted head, set rules).  The metric is scored
+candidate tokens per second of the full-vocabulary pass (512 per step); the
+step time includes the restricted pass.
+
+Printed: one JSON line (rank 0).  Timing: CUDA events on the launching stream,
+after warm-up, synchronised on both sides; W (1.27 GB) is larger than L2, so
+consecutive steps do not hit in L2 for the dominant stream.  Kernel-level
+times come from event pairs the library records around its own launches.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+                  [--workload binary|multitoken|wideschema|large|tiny]
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "candidate tokens scored/sec (full-vocab log-softmax) and % of roofline, 1 GB300"
+UNIT = "tokens/s"
+
+WORKLOADS = {
+    # name: (generator, modes per step, default steps, description)
+    "binary": ("binary_batch", ("full", "restricted"), 6000,
+               "binary single-token batch: 256 questions x {A,B} codes, d=2560, V=248320; "
+               "full vocabulary (T=1) + restricted 26-code union (T=2.179)"),
+    "multitoken": ("multi_token_choice", ("full",), 300,
+                   "multi-token choice: 64 questions x K=8, 1-12 tokens, d=1536, V=262144, T=1"),
+    "wideschema": ("wide_schema", ("full",), 60,
+                   "wide schema: 16 requests x 32 fields, enum K 2-26 / ordinal K=5, d=2560, V=248320, T=2.179"),
+    "large": ("large_choice", ("full",), 40,
+              "large choice: 16 requests x K=64, 8-32 tokens, d=4096, V=152064, T=1"),
+    "tiny": ("tiny", ("full",), 2000, "tiny: d=64, V=1000, 3 sets"),
+}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+def head_source_hash():
+    h = hashlib.sha256()
+    for f in ("k_head.cu", "jet_internal.cuh"):
+        h.update(open(os.path.join(ROOT, "candidate_answer_scoring_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(workload):
+    """DRAM bytes per head launch from a committed ncu summary, if it was taken
+    on the current head-kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "head_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    e = d.get(workload)
+    if not e or e.get("source_hash") != head_source_hash():
+        return None
+    return float(e["dram_bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.rows = []
+        self.proc = None
+        self.gpu_id = gpu_id
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if self.gpu_id is not None:
+            cmd += ["-i", str(self.gpu_id)]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in self.rows for n, v in zip(names, r[4:8]) if v.lower() == "active"})
+        pw = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows),
+                "power_w_max": max(pw) if pw else None}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def make_workload(name, rank=0):
+    import workloads as wk
+    gen = getattr(wk, WORKLOADS[name][0])
+    wl = gen()
+    steps = []
+    for mode in WORKLOADS[name][1]:
+        if mode == "full":
+            steps.append(wl)
+        else:
+            steps.append(wk.binary_restricted(base=wl))
+    return wl, steps
+
+
+def roofline_terms(wl, peaks, sustained):
+    """Algorithmic work of one full-vocabulary head launch and the roofline time."""
+    N, d, V, n_tok = wl.N, wl.d, wl.V, wl.n_tok
+    flops = 2.0 * N * d * V
+    bytes_ = 2.0 * V * d + 2.0 * N * d + 8.0 * n_tok
+    tc = (peaks["bf16_sustained"] if sustained else peaks["bf16"]) * 1e12
+    t_tc = flops / tc
+    t_hbm = bytes_ / (peaks["hbm"] * 1e9)
+    return flops, bytes_, t_tc, t_hbm
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (reference arm and cpu_baseline)
+# ---------------------------------------------------------------------------
+def _subset(wl, n_sets):
+    import numpy as np
+    import workloads as wk
+    k = min(n_sets, wl.n_sets)
+    c1 = int(wl.set_offsets[k])
+    t1 = int(wl.cand_offsets[c1])
+    rows, new_row = np.unique(wl.tok_row[:t1], return_inverse=True)
+    return wk.Workload(wl.name + f"-first{k}", wl.d, wl.V, np.ascontiguousarray(wl.H[rows]), wl.W,
+                       new_row.astype(np.int32), wl.tok_ids[:t1].copy(), wl.cand_offsets[:c1 + 1].copy(),
+                       wl.set_offsets[:k + 1].copy(), wl.kind[:k].copy(), wl.T, wl.mode, wl.union_ids,
+                       dict(wl.info))
+
+
+def time_oracle(steps_wl, n_sets, repeats=1):
+    """Run the oracle on the first n_sets sets of each step workload; returns
+    (seconds per step, full-mode tokens per step, threads)."""
+    import oracle
+    subs = [_subset(w, n_sets) for w in steps_wl]
+    t0 = time.perf_counter()
+    for _ in range(repeats):
+        for s in subs:
+            oracle.score_workload(s)
+    dt = (time.perf_counter() - t0) / repeats
+    return dt, subs[0].n_tok, oracle.max_threads()
+
+
+def reference_arm(args, world, rank):
+    if rank != 0:
+        return 0
+    name = args.workload
+    wl, steps_wl = make_workload(name)
+    import oracle
+    oracle.build()
+    # size one step to about 2 s of oracle work, then cap the whole run at ~3 min
+    probe_sets = 1
+    dt1, _, _ = time_oracle(steps_wl, probe_sets)
+    per_set = max(dt1 / probe_sets, 1e-4)
+    n_sets = max(1, min(wl.n_sets, int(2.0 / per_set)))
+    K = args.steps if args.steps is not None else 5
+    W = args.warmup if args.warmup is not None else 1
+    budget = 180.0
+    step_est = per_set * n_sets
+    k_run = max(1, min(K, int(budget / max(step_est, 1e-3)) - W))
+    for _ in range(W):
+        time_oracle(steps_wl, n_sets)
+    t0 = time.perf_counter()
+    tokens = 0
+    threads = 1
+    for _ in range(k_run):
+        dt, ntok, threads = time_oracle(steps_wl, n_sets)
+        tokens += ntok
+    el = time.perf_counter() - t0
+    value = tokens / el
+    sample = (f"first {n_sets} of {wl.n_sets} sets per step ({_subset(wl, n_sets).n_tok} full-vocab tokens"
+              f"{' + the same sets restricted' if len(steps_wl) > 1 else ''}); fp64 C oracle, OpenMP over rows")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": k_run, "steps_requested": K, "warmup": W, "ms_per_step": 1e3 * el / k_run,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOADS[name][3]},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def gpu_arm(args, world, rank, local):
+    import numpy as np
+    import torch
+
+    import candidate_answer_scoring_gb300 as jet
+    from candidate_answer_scoring_gb300 import build as libbuild
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    libbuild.build()
+    peaks = load_peaks()
+
+    name = args.workload
+    wl, steps_wl = make_workload(name, rank)
+    K = args.steps if args.steps is not None else WORKLOADS[name][2]
+    W = args.warmup if args.warmup is not None else 10
+    W = max(W, 3)
+
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    Wd = t(wl.W.view(np.int16)).view(torch.bfloat16)
+    ins = []
+    for s in steps_wl:
+        ins.append(dict(H=t(s.H.view(np.int16)).view(torch.bfloat16), tok_row=t(s.tok_row), tok_ids=t(s.tok_ids),
+                        cand_offsets=t(s.cand_offsets), set_offsets=t(s.set_offsets), kind=t(s.kind),
+                        union_ids=None if s.union_ids is None else t(s.union_ids), T=s.T, mode=s.mode, wl=s))
+    sc = jet.JetScorer(wl.d, wl.V, wl.N, wl.n_tok, device=local)
+    outs = [sc.alloc_outputs(s.N, s.n_tok, s.n_cand, s.n_sets) for s in steps_wl]
+    stream = torch.cuda.Stream(dev)
+
+    def step():
+        for x, o in zip(ins, outs):
+            sc.score_sets(x["H"], Wd, x["tok_row"], x["tok_ids"], x["cand_offsets"], x["set_offsets"], x["kind"],
+                          x["T"], x["mode"], x["union_ids"], out=o, sync=False)
+
+    with torch.cuda.stream(stream):
+        for _ in range(W):
+            step()
+        rc = sc.sync_status()
+        if rc != 0:
+            raise RuntimeError(f"device status {rc} ({jet.status_string(rc)}) after warm-up")
+        torch.cuda.synchronize(dev)
+
+        gpu_uuid = None
+        try:
+            gpu_uuid = str(torch.cuda.get_device_properties(dev).uuid)
+            if not gpu_uuid.startswith("GPU-"):
+                gpu_uuid = "GPU-" + gpu_uuid
+        except Exception:
+            gpu_uuid = None
+        clocks = ClockSampler(gpu_uuid)
+        clocks.start()
+        time.sleep(0.3)
+        sc.profile(True)
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            torch.distributed.barrier()
+        prof = sc.profile_read()
+        sc.profile(False)
+        clk = clocks.stop()
+        rc = sc.sync_status()
+        if rc != 0:
+            raise RuntimeError(f"device status {rc} ({jet.status_string(rc)}) in the timed region")
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
+    tokens_per_step = steps_wl[0].n_tok
+    value = world * tokens_per_step * K / (ms / 1e3)
+    ms_step = ms / K
+
+    # kernel roofline: the full-vocabulary head
+    head = prof["head"]
+    head_ms = head["ms"] / max(1, head["launches"])
+    flops, bytes_, t_tc, t_hbm = roofline_terms(wl, peaks, sustained=True)
+    _, _, t_tc_burst, _ = roofline_terms(wl, peaks, sustained=False)
+    # bound by the roofline formula with the burst tensor peak; the tensor
+    # denominator is the sustained peak, since the head runs inside a long loop
+    bound = "hbm" if t_hbm >= t_tc_burst else "tensor"
+    if bound == "hbm":
+        achieved = bytes_ / (head_ms / 1e3) / 1e9
+        peak, unit = peaks["hbm"], "GB/s"
+    else:
+        achieved = flops / (head_ms / 1e3) / 1e12
+        peak, unit = peaks["bf16_sustained"], "TFLOP/s"
+    launches = sum(v["launches"] for k, v in prof.items() if isinstance(v, dict))
+    t_roof = max(t_tc, t_hbm)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {
+            "workload": WORKLOADS[name][3], "d": wl.d, "V": wl.V, "N": wl.N, "n_tok": wl.n_tok,
+            "n_cand": wl.n_cand, "n_sets": wl.n_sets, "modes": list(WORKLOADS[name][1]),
+            "parallelism": f"replicas x{world}",
+            "l2": "inputs larger than L2 (W = %.2f GB > 129 MB L2)" % (wl.W.nbytes / 1e9),
+            "accumulate": "fp32 (tcgen05 bf16 x bf16 -> fp32 TMEM)",
+            "plan": sc.plan_info(wl.N),
+            "step_roofline_us": t_roof * 1e6, "step_roofline_frac": t_roof / (ms_step / 1e3),
+            "kernel_ms_per_step": {k: v["ms"] / K for k, v in prof.items() if isinstance(v, dict)},
+            "peaks": peaks["source"],
+        },
+        "gpu_launches": int(launches),
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                     "frac": achieved / peak, "traffic": committed_traffic(name),
+                     "kernel": "head_lse_gather (tcgen05)", "kernel_ms": head_ms,
+                     "algorithmic_bytes": bytes_, "algorithmic_flops": flops,
+                     "t_tensor_us_sustained": t_tc * 1e6, "t_tensor_us_burst": t_tc_burst * 1e6,
+                     "t_hbm_us": t_hbm * 1e6, "peak_note": "of measured" if peaks["source"] == "measured"
+                     else "of fallback"},
+        "clocks": clk,
+    }
+
+    # end to end through the public API with host buffers (pinned)
+    if not args.no_e2e:
+        pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+        hins = []
+        h2d = d2h = 0
+        for s in steps_wl:
+            hi = dict(H=pin(s.H.view(np.int16)).view(torch.bfloat16), tok_row=pin(s.tok_row), tok_ids=pin(s.tok_ids),
+                      cand_offsets=pin(s.cand_offsets), set_offsets=pin(s.set_offsets), kind=pin(s.kind),
+                      union_ids=None if s.union_ids is None else pin(s.union_ids), T=s.T, mode=s.mode)
+            hins.append(hi)
+            h2d += sum(v.numel() * v.element_size() for k, v in hi.items() if isinstance(v, torch.Tensor))
+            ho = {k: torch.empty(n, dtype=torch.int32 if k == "decision" else torch.float32).pin_memory()
+                  for k, n in (("q", s.n_cand), ("decision", s.n_sets), ("expected", s.n_sets),
+                               ("confidence", s.n_sets), ("mass", s.n_sets))}
+            hi["out"] = ho
+            d2h += sum(v.numel() * 4 for v in ho.values())
+        Ke = max(3, min(K, 500))
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                for hi in hins:
+                    sc.score_sets_host(hi["H"], Wd, hi["tok_row"], hi["tok_ids"], hi["cand_offsets"],
+                                       hi["set_offsets"], hi["kind"], hi["T"], hi["mode"], hi["union_ids"],
+                                       out=hi["out"])
+            torch.cuda.synchronize(dev)
+            t0 = time.perf_counter()
+            for _ in range(Ke):
+                for hi in hins:
+                    sc.score_sets_host(hi["H"], Wd, hi["tok_row"], hi["tok_ids"], hi["cand_offsets"],
+                                       hi["set_offsets"], hi["kind"], hi["T"], hi["mode"], hi["union_ids"],
+                                       out=hi["out"])
+            torch.cuda.synchronize(dev)
+            el = time.perf_counter() - t0
+        if world > 1:
+            tt = torch.tensor([el], device=dev)
+            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+            el = float(tt.item())
+        line["e2e"] = {"value": world * tokens_per_step * Ke / el, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                       "d2h_bytes_per_step": d2h, "steps": Ke, "ms_per_step": 1e3 * el / Ke,
+                       "note": "jet_score_sets_host per mode: pinned host inputs -> device -> host results; "
+                               "W resident on the device like any model weight"}
+
+    # CPU oracle baseline on a bounded sample (rank 0, one GPU only)
+    if world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        dt1, _, _ = time_oracle(steps_wl, 1)
+        n_sets = max(1, min(wl.n_sets, int(15.0 / max(dt1, 1e-4))))
+        dt, ntok, threads = time_oracle(steps_wl, n_sets)
+        line["cpu_baseline"] = {
+            "value": ntok / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"first {n_sets} of {wl.n_sets} sets ({ntok} full-vocab tokens"
+                      f"{', plus the restricted pass' if len(steps_wl) > 1 else ''}); {dt:.1f} s",
+        }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    sc.close()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="binary", choices=sorted(WORKLOADS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        return reference_arm(args, world, rank)
+    return gpu_arm(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,11 @@
+"""libjetscore: the candidate-set scoring head on one GB300 (sm_103a).
+
+Hidden rows at teacher-forced candidate positions are projected onto the full
+vocabulary inside a tcgen05/TMEM kernel that keeps a running log-sum-exp and
+gathers only the supplied tokens' logits; candidate log-likelihoods, the set
+softmax with temperature, the argmax decision, the expected index, confidence
+and allowed-token mass follow in small kernels.  ``JetScorer`` is the Python
+face of the C ABI in ``include/jetscore.h``.
+"""
+from .jetscore import (JET_KIND_BINARY, JET_KIND_CHOICE, JET_KIND_ORDINAL, JET_MODE_FULL,  # noqa: F401
+                       JET_MODE_RESTRICTED, JetError, JetScorer, load, status_string)

@@ -1,0 +1,574 @@
+// C ABI of libjetscore: context and workspace, host-side argument checks, the
+// vocabulary-split schedule, TMA tensor maps, and the launch sequence
+//   pre-pass -> head (full vocabulary) or restricted head -> merge -> set rules.
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "jet_internal.cuh"
+
+using namespace jet;
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+constexpr int UNITS_PER_SM_CAP = 64;   // bound on schedule units (partials workspace)
+
+template <class T>
+cudaError_t dalloc(T** p, size_t n) {
+  return cudaMalloc(reinterpret_cast<void**>(p), (n ? n : 1) * sizeof(T));
+}
+
+}  // namespace
+
+struct jet_ctx {
+  int device = 0, d = 0, V = 0, max_rows = 0, max_tokens = 0, num_sms = 0, units_cap = 0;
+  EncodeTiledFn encode = nullptr;
+  // device workspace
+  int* err = nullptr;
+  int* row_ptr = nullptr;
+  int* row_cur = nullptr;
+  int2* row_list = nullptr;
+  int* upos = nullptr;
+  float* zg = nullptr;
+  float2* part = nullptr;
+  unsigned long long* hash = nullptr;
+  // scratch for outputs the caller did not ask for
+  float *lse = nullptr, *logp = nullptr, *s = nullptr, *q = nullptr, *qe = nullptr;
+  int32_t* dec = nullptr;
+  float *expd = nullptr, *conf = nullptr, *mass = nullptr;
+  // device staging of host inputs (jet_score_sets_host)
+  uint16_t* stH = nullptr;
+  int32_t *st_row = nullptr, *st_tok = nullptr, *st_co = nullptr, *st_so = nullptr, *st_union = nullptr;
+  uint8_t* st_kind = nullptr;
+  int* h_err = nullptr;   // pinned
+  // schedule cache
+  int plan_rows = -1;
+  Plan plan;
+  // kernel timing (jet_profile_enable)
+  bool prof = false;
+  std::vector<cudaEvent_t> ev[5];   // pairs: start, stop
+  size_t ev_used[5] = {0, 0, 0, 0, 0};
+  double launches[5] = {0, 0, 0, 0, 0};
+  double untimed = 0;
+};
+
+namespace {
+
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = true;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    if (prev != dev) ok = (cudaSetDevice(dev) == cudaSuccess);
+  }
+  ~DeviceGuard() {
+    int cur;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+// Choose the number of vocabulary splits S per row tile: every unit is one row
+// tile over n_vt/S vocabulary tiles, units run G at a time, so the busiest CTA
+// processes ceil(n_mt*S/G) * ceil(n_vt/S) tiles; take the smallest such count
+// (ties: fewer splits).  Bands of Gm row tiles keep Gm H tiles (128*d*2 bytes
+// each) within ~48 MB of L2 while the band's units stream W.
+Plan make_plan(int N, int V, int d, int G, int units_cap) {
+  Plan p;
+  p.n_mt = (N + BM - 1) / BM;
+  p.n_vt = (V + BN - 1) / BN;
+  const int S_max = std::max(1, std::min(p.n_vt, units_cap / std::max(1, p.n_mt)));
+  long long best = -1;
+  for (int S = 1; S <= S_max; ++S) {
+    const long long waves = ((long long)p.n_mt * S + G - 1) / G;
+    const long long t = waves * ((p.n_vt + S - 1) / S);
+    if (best < 0 || t < best) { best = t; p.S = S; }
+  }
+  const long long a_tile = (long long)BM * d * 2;
+  const int gm_max = (int)std::max(1LL, (48LL << 20) / a_tile);
+  p.Gm = std::max(1, std::min(p.n_mt, gm_max));
+  p.n_full_bands = p.n_mt / p.Gm;
+  p.r_last = p.n_mt - p.n_full_bands * p.Gm;
+  p.units = p.n_mt * p.S;
+  p.grid = std::min(p.units, G);
+  return p;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? JET_OK : JET_ERR_CUDA; }
+
+enum { K_PREP = 0, K_HEAD = 1, K_MERGE = 2, K_RESTRICTED = 3, K_SETS = 4 };
+constexpr size_t PROF_PAIRS = 65536;
+
+// Event pair around one launch when timing is on; returns the pair's slot or -1.
+long prof_begin(jet_ctx* c, int kind, cudaStream_t st) {
+  if (!c->prof) return -1;
+  c->launches[kind] += 1;
+  std::vector<cudaEvent_t>& v = c->ev[kind];
+  if (c->ev_used[kind] + 2 > 2 * PROF_PAIRS) { c->untimed += 1; return -1; }
+  while (v.size() < c->ev_used[kind] + 2) {
+    cudaEvent_t e;
+    if (cudaEventCreate(&e) != cudaSuccess) { c->untimed += 1; return -1; }
+    v.push_back(e);
+  }
+  const long slot = (long)c->ev_used[kind];
+  c->ev_used[kind] += 2;
+  cudaEventRecord(v[slot], st);
+  return slot;
+}
+
+void prof_end(jet_ctx* c, int kind, long slot, cudaStream_t st) {
+  if (slot >= 0) cudaEventRecord(c->ev[kind][slot + 1], st);
+}
+
+struct ProfScope {
+  jet_ctx* c; int kind; long slot; cudaStream_t st;
+  ProfScope(jet_ctx* c_, int k, cudaStream_t s) : c(c_), kind(k), slot(prof_begin(c_, k, s)), st(s) {}
+  ~ProfScope() { prof_end(c, kind, slot, st); }
+};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int encode_kmajor(jet_ctx* c, CUtensorMap* map, const void* base, int rows, int box_rows) {
+  const cuuint64_t dims[2] = {(cuuint64_t)c->d, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)c->d * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = c->encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? JET_OK : JET_ERR_CUDA;
+}
+
+const Plan& plan_for(jet_ctx* c, int n_rows) {
+  if (c->plan_rows != n_rows) {
+    c->plan = make_plan(n_rows, c->V, c->d, c->num_sms, c->units_cap);
+    c->plan_rows = n_rows;
+  }
+  return c->plan;
+}
+
+// Full-vocabulary log-probabilities for the rows/tokens the pre-pass listed.
+int run_full_head(jet_ctx* c, const void* H, const void* W, int n_rows, float* logp, float* lse,
+                  cudaStream_t st) {
+  CUtensorMap tmH, tmW;
+  int rc = encode_kmajor(c, &tmH, H, n_rows, BM);
+  if (rc != JET_OK) return rc;
+  rc = encode_kmajor(c, &tmW, W, c->V, BN);
+  if (rc != JET_OK) return rc;
+  HeadArgs ha;
+  ha.N = n_rows;
+  ha.V = c->V;
+  ha.d = c->d;
+  ha.plan = plan_for(c, n_rows);
+  ha.row_ptr = c->row_ptr;
+  ha.row_list = c->row_list;
+  ha.zg = c->zg;
+  ha.part = c->part;
+  ha.err = c->err;
+  cudaError_t e;
+  {
+    ProfScope ps(c, K_HEAD, st);
+    e = launch_head(tmH, tmW, ha, st);
+  }
+  if (e != cudaSuccess) return JET_ERR_CUDA;
+  MergeArgs ma;
+  ma.N = n_rows;
+  ma.plan = ha.plan;
+  ma.part = c->part;
+  ma.zg = c->zg;
+  ma.row_ptr = c->row_ptr;
+  ma.row_list = c->row_list;
+  ma.lse = lse;
+  ma.logp = logp;
+  ma.err = c->err;
+  ProfScope ps(c, K_MERGE, st);
+  return cuda_status(launch_merge(ma, st));
+}
+
+int check_sets_args(jet_ctx* c, const void* H, const void* W, int n_rows, const int32_t* tok_row,
+                    const int32_t* tok_ids, int n_tok, const int32_t* cand_offsets, int n_cand,
+                    const int32_t* set_offsets, const uint8_t* kind, int n_sets, float T, int mode,
+                    const int32_t* union_ids, int n_union) {
+  if (!c) return JET_ERR_ARG;
+  if (n_rows < 0 || n_tok < 0 || n_cand < 0 || n_sets < 0) return JET_ERR_ARG;
+  if (!(T > 0.f) || !std::isfinite(T)) return JET_ERR_ARG;
+  if (mode != JET_MODE_FULL && mode != JET_MODE_RESTRICTED) return JET_ERR_MODE;
+  if (n_tok == 0) return (n_cand == 0 && n_sets == 0) ? JET_OK : JET_ERR_OFFSETS;
+  if (n_cand < 1 || n_sets < 1 || n_cand > n_tok || n_sets > n_cand) return JET_ERR_OFFSETS;
+  if (n_rows < 1) return JET_ERR_ARG;
+  if (n_rows > c->max_rows || n_tok > c->max_tokens) return JET_ERR_WORKSPACE;
+  if (!H || !W || !tok_row || !tok_ids || !cand_offsets || !set_offsets || !kind) return JET_ERR_ARG;
+  if (!aligned16(H) || !aligned16(W)) return JET_ERR_ARG;
+  if (mode == JET_MODE_RESTRICTED && (!union_ids || n_union < 1 || n_union > JET_MAX_UNION)) return JET_ERR_ARG;
+  return JET_OK;
+}
+
+int score_sets_enqueue(jet_ctx* c, const void* H, const void* W, int n_rows, const int32_t* tok_row,
+                       const int32_t* tok_ids, int n_tok, const int32_t* cand_offsets, int n_cand,
+                       const int32_t* set_offsets, const uint8_t* kind, int n_sets, float T, int mode,
+                       const int32_t* union_ids, int n_union, const jet_set_out* out, cudaStream_t st) {
+  jet_set_out o;
+  std::memset(&o, 0, sizeof o);
+  if (out) o = *out;
+  float* logp = o.logp ? o.logp : c->logp;
+  float* lse = o.lse;
+
+  PrepArgs pa;
+  pa.n_rows = n_rows;
+  pa.n_tok = n_tok;
+  pa.V = c->V;
+  pa.tok_row = tok_row;
+  pa.tok_ids = tok_ids;
+  pa.cand_offsets = cand_offsets;
+  pa.n_cand = n_cand;
+  pa.set_offsets = set_offsets;
+  pa.kind = kind;
+  pa.n_sets = n_sets;
+  pa.mode = mode;
+  pa.union_ids = union_ids;
+  pa.n_union = mode == JET_MODE_RESTRICTED ? n_union : 0;
+  pa.row_ptr = c->row_ptr;
+  pa.row_cur = c->row_cur;
+  pa.row_list = c->row_list;
+  pa.upos = c->upos;
+  pa.err = c->err;
+  {
+    ProfScope ps(c, K_PREP, st);
+    if (launch_prep(pa, st) != cudaSuccess) return JET_ERR_CUDA;
+  }
+
+  int rc;
+  if (mode == JET_MODE_FULL) {
+    rc = run_full_head(c, H, W, n_rows, logp, lse, st);
+  } else {
+    RestrictedArgs ra;
+    ra.N = n_rows;
+    ra.d = c->d;
+    ra.n_union = n_union;
+    ra.H = static_cast<const uint16_t*>(H);
+    ra.W = static_cast<const uint16_t*>(W);
+    ra.union_ids = union_ids;
+    ra.row_ptr = c->row_ptr;
+    ra.row_list = c->row_list;
+    ra.upos = c->upos;
+    ra.lse = lse;
+    ra.logp = logp;
+    ra.err = c->err;
+    ProfScope ps(c, K_RESTRICTED, st);
+    rc = cuda_status(launch_restricted(ra, st));
+  }
+  if (rc != JET_OK) return rc;
+
+  SetArgs sa;
+  sa.n_sets = n_sets;
+  sa.logp = logp;
+  sa.tok_ids = tok_ids;
+  sa.cand_offsets = cand_offsets;
+  sa.set_offsets = set_offsets;
+  sa.T = T;
+  sa.s = o.s ? o.s : c->s;
+  sa.q = o.q ? o.q : c->q;
+  sa.q_equiv = o.q_equiv ? o.q_equiv : c->qe;
+  sa.decision = o.decision ? o.decision : c->dec;
+  sa.expected = o.expected ? o.expected : c->expd;
+  sa.confidence = o.confidence ? o.confidence : c->conf;
+  sa.mass = o.mass ? o.mass : c->mass;
+  sa.hash = c->hash;
+  sa.err = c->err;
+  ProfScope ps(c, K_SETS, st);
+  return cuda_status(launch_sets(sa, st));
+}
+
+int read_status(jet_ctx* c, cudaStream_t st) {
+  if (cudaMemcpyAsync(c->h_err, c->err, ERR_WORDS * sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return JET_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return JET_ERR_CUDA;
+  return c->h_err[0];
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* jet_status_string(int status) {
+  switch (status) {
+    case JET_OK: return "ok";
+    case JET_ERR_ARG: return "invalid argument";
+    case JET_ERR_TOKEN_RANGE: return "token id or row index out of range";
+    case JET_ERR_OFFSETS: return "invalid candidate or set offsets";
+    case JET_ERR_MODE: return "invalid mode, or multi-token candidate in restricted mode";
+    case JET_ERR_NOT_IN_UNION: return "candidate token not in the union, or repeated union id";
+    case JET_ERR_WORKSPACE: return "batch larger than the context workspace";
+    case JET_ERR_UNSUPPORTED: return "device is not a GB300 (sm_103)";
+    case JET_ERR_CUDA: return "CUDA runtime error";
+    case JET_ERR_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int jet_create(jet_ctx** out, int d, int V, int max_rows, int max_tokens, int device) {
+  if (!out) return JET_ERR_ARG;
+  *out = nullptr;
+  if (d < 64 || d > 16384 || d % 64 != 0 || V < 1 || max_rows < 1 || max_tokens < 1) return JET_ERR_ARG;
+  DeviceGuard g(device);
+  if (!g.ok) return JET_ERR_CUDA;
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return JET_ERR_CUDA;
+  if (prop.major != 10 || prop.minor != 3) return JET_ERR_UNSUPPORTED;
+
+  jet_ctx* c = new (std::nothrow) jet_ctx;
+  if (!c) return JET_ERR_CUDA;
+  c->device = device;
+  c->d = d;
+  c->V = V;
+  c->max_rows = max_rows;
+  c->max_tokens = max_tokens;
+  c->num_sms = prop.multiProcessorCount;
+  c->units_cap = std::max(UNITS_PER_SM_CAP * c->num_sms, (max_rows + BM - 1) / BM);
+
+  cudaDriverEntryPointQueryResult q;
+  void* fn = nullptr;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+          cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn) {
+    delete c;
+    return JET_ERR_CUDA;
+  }
+  c->encode = reinterpret_cast<EncodeTiledFn>(fn);
+
+  const size_t R = (size_t)max_rows, Tk = (size_t)max_tokens;
+  cudaError_t e = cudaSuccess;
+  auto A = [&](cudaError_t r) { if (e == cudaSuccess) e = r; };
+  A(dalloc(&c->err, ERR_WORDS));
+  A(dalloc(&c->row_ptr, R + 1));
+  A(dalloc(&c->row_cur, R + 1));
+  A(dalloc(&c->row_list, Tk));
+  A(dalloc(&c->upos, Tk));
+  A(dalloc(&c->zg, Tk));
+  A(dalloc(&c->part, (size_t)c->units_cap * 2 * BM));
+  A(dalloc(&c->hash, Tk));
+  A(dalloc(&c->lse, R));
+  A(dalloc(&c->logp, Tk));
+  A(dalloc(&c->s, Tk));
+  A(dalloc(&c->q, Tk));
+  A(dalloc(&c->qe, Tk));
+  A(dalloc(&c->dec, Tk));
+  A(dalloc(&c->expd, Tk));
+  A(dalloc(&c->conf, Tk));
+  A(dalloc(&c->mass, Tk));
+  A(dalloc(&c->stH, R * (size_t)d));
+  A(dalloc(&c->st_row, Tk));
+  A(dalloc(&c->st_tok, Tk));
+  A(dalloc(&c->st_co, Tk + 1));
+  A(dalloc(&c->st_so, Tk + 1));
+  A(dalloc(&c->st_kind, Tk));
+  A(dalloc(&c->st_union, (size_t)JET_MAX_UNION));
+  A(cudaMallocHost(reinterpret_cast<void**>(&c->h_err), ERR_WORDS * sizeof(int)));
+  A(cudaMemset(c->err, 0, ERR_WORDS * sizeof(int)));
+  if (e != cudaSuccess) {
+    jet_destroy(c);
+    return JET_ERR_CUDA;
+  }
+  *out = c;
+  return JET_OK;
+}
+
+void jet_destroy(jet_ctx* c) {
+  if (!c) return;
+  DeviceGuard g(c->device);
+  cudaDeviceSynchronize();
+  void* ptrs[] = {c->err, c->row_ptr, c->row_cur, c->row_list, c->upos, c->zg, c->part, c->hash,
+                  c->lse, c->logp, c->s, c->q, c->qe, c->dec, c->expd, c->conf, c->mass, c->stH,
+                  c->st_row, c->st_tok, c->st_co, c->st_so, c->st_kind, c->st_union};
+  for (void* p : ptrs)
+    if (p) cudaFree(p);
+  for (auto& v : c->ev)
+    for (cudaEvent_t e : v) cudaEventDestroy(e);
+  if (c->h_err) cudaFreeHost(c->h_err);
+  delete c;
+}
+
+int jet_profile_enable(jet_ctx* c, int enable) {
+  if (!c) return JET_ERR_ARG;
+  c->prof = enable != 0;
+  return JET_OK;
+}
+
+int jet_profile_read(jet_ctx* c, double* out, int n_out) {
+  if (!c || !out || n_out < 10) return JET_ERR_ARG;
+  DeviceGuard g(c->device);
+  if (!g.ok) return JET_ERR_CUDA;
+  int rc = JET_OK;
+  for (int k = 0; k < 5; ++k) {
+    double ms_total = 0;
+    for (size_t i = 0; i + 1 < c->ev_used[k]; i += 2) {
+      float ms = 0.f;
+      if (cudaEventSynchronize(c->ev[k][i + 1]) != cudaSuccess ||
+          cudaEventElapsedTime(&ms, c->ev[k][i], c->ev[k][i + 1]) != cudaSuccess) {
+        rc = JET_ERR_CUDA;
+        continue;
+      }
+      ms_total += ms;
+    }
+    out[2 * k] = c->launches[k];
+    out[2 * k + 1] = ms_total;
+    c->ev_used[k] = 0;
+    c->launches[k] = 0;
+  }
+  if (n_out > 10) out[10] = c->untimed;
+  c->untimed = 0;
+  return rc;
+}
+
+int jet_plan_info(jet_ctx* c, int n_rows, int* info) {
+  if (!c || !info || n_rows < 1 || n_rows > c->max_rows) return JET_ERR_ARG;
+  const Plan& p = plan_for(c, n_rows);
+  const int v[8] = {p.n_mt, p.n_vt, p.S, p.Gm, p.units, p.grid, BM, BN};
+  std::memcpy(info, v, sizeof v);
+  return JET_OK;
+}
+
+int jet_score_sets_async(jet_ctx* c, const void* H, const void* W, int n_rows, const int32_t* tok_row,
+                         const int32_t* tok_ids, int n_tok, const int32_t* cand_offsets, int n_cand,
+                         const int32_t* set_offsets, const uint8_t* kind, int n_sets, float T, int mode,
+                         const int32_t* union_ids, int n_union, const jet_set_out* out, void* stream) {
+  int rc = check_sets_args(c, H, W, n_rows, tok_row, tok_ids, n_tok, cand_offsets, n_cand, set_offsets, kind,
+                           n_sets, T, mode, union_ids, n_union);
+  if (rc != JET_OK || n_tok == 0) return rc;
+  DeviceGuard g(c->device);
+  if (!g.ok) return JET_ERR_CUDA;
+  return score_sets_enqueue(c, H, W, n_rows, tok_row, tok_ids, n_tok, cand_offsets, n_cand, set_offsets, kind,
+                            n_sets, T, mode, union_ids, n_union, out, static_cast<cudaStream_t>(stream));
+}
+
+int jet_sync_status(jet_ctx* c, void* stream) {
+  if (!c) return JET_ERR_ARG;
+  DeviceGuard g(c->device);
+  if (!g.ok) return JET_ERR_CUDA;
+  return read_status(c, static_cast<cudaStream_t>(stream));
+}
+
+int jet_score_sets(jet_ctx* c, const void* H, const void* W, int n_rows, const int32_t* tok_row,
+                   const int32_t* tok_ids, int n_tok, const int32_t* cand_offsets, int n_cand,
+                   const int32_t* set_offsets, const uint8_t* kind, int n_sets, float T, int mode,
+                   const int32_t* union_ids, int n_union, const jet_set_out* out, void* stream) {
+  int rc = check_sets_args(c, H, W, n_rows, tok_row, tok_ids, n_tok, cand_offsets, n_cand, set_offsets, kind,
+                           n_sets, T, mode, union_ids, n_union);
+  if (rc != JET_OK || n_tok == 0) return rc;
+  DeviceGuard g(c->device);
+  if (!g.ok) return JET_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  rc = score_sets_enqueue(c, H, W, n_rows, tok_row, tok_ids, n_tok, cand_offsets, n_cand, set_offsets, kind,
+                          n_sets, T, mode, union_ids, n_union, out, st);
+  if (rc != JET_OK) {
+    cudaStreamSynchronize(st);
+    return rc;
+  }
+  return read_status(c, st);
+}
+
+int jet_score_tokens(jet_ctx* c, const void* H, const void* W, const int32_t* tok_ids, int n_pos, float* logp,
+                     float* lse, void* stream) {
+  if (!c || n_pos < 0) return JET_ERR_ARG;
+  if (n_pos == 0) return JET_OK;
+  if (!H || !W || !tok_ids || !logp || !aligned16(H) || !aligned16(W)) return JET_ERR_ARG;
+  if (n_pos > c->max_rows || n_pos > c->max_tokens) return JET_ERR_WORKSPACE;
+  DeviceGuard g(c->device);
+  if (!g.ok) return JET_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  PrepArgs pa;
+  std::memset(&pa, 0, sizeof pa);
+  pa.n_rows = n_pos;
+  pa.n_tok = n_pos;
+  pa.V = c->V;
+  pa.tok_row = nullptr;   // token i is predicted by row i
+  pa.tok_ids = tok_ids;
+  pa.mode = JET_MODE_FULL;
+  pa.row_ptr = c->row_ptr;
+  pa.row_cur = c->row_cur;
+  pa.row_list = c->row_list;
+  pa.upos = c->upos;
+  pa.err = c->err;
+  {
+    ProfScope ps(c, K_PREP, st);
+    if (launch_prep(pa, st) != cudaSuccess) return JET_ERR_CUDA;
+  }
+  int rc = run_full_head(c, H, W, n_pos, logp, lse, st);
+  if (rc != JET_OK) {
+    cudaStreamSynchronize(st);
+    return rc;
+  }
+  return read_status(c, st);
+}
+
+int jet_score_sets_host(jet_ctx* c, const void* H, const void* W, int n_rows, const int32_t* tok_row,
+                        const int32_t* tok_ids, int n_tok, const int32_t* cand_offsets, int n_cand,
+                        const int32_t* set_offsets, const uint8_t* kind, int n_sets, float T, int mode,
+                        const int32_t* union_ids, int n_union, const jet_set_out* out_host, void* stream) {
+  int rc = check_sets_args(c, H, W, n_rows, tok_row, tok_ids, n_tok, cand_offsets, n_cand, set_offsets, kind,
+                           n_sets, T, mode, union_ids, n_union);
+  if (rc != JET_OK || n_tok == 0) return rc;
+  DeviceGuard g(c->device);
+  if (!g.ok) return JET_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  auto H2D = [&](void* dst, const void* src, size_t bytes) {
+    if (e == cudaSuccess && bytes) e = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, st);
+  };
+  H2D(c->stH, H, (size_t)n_rows * c->d * 2);
+  H2D(c->st_row, tok_row, (size_t)n_tok * 4);
+  H2D(c->st_tok, tok_ids, (size_t)n_tok * 4);
+  H2D(c->st_co, cand_offsets, (size_t)(n_cand + 1) * 4);
+  H2D(c->st_so, set_offsets, (size_t)(n_sets + 1) * 4);
+  H2D(c->st_kind, kind, (size_t)n_sets);
+  const int32_t* dev_union = nullptr;
+  if (mode == JET_MODE_RESTRICTED) {
+    H2D(c->st_union, union_ids, (size_t)n_union * 4);
+    dev_union = c->st_union;
+  }
+  if (e != cudaSuccess) return JET_ERR_CUDA;
+  jet_set_out dev;
+  dev.logp = c->logp;
+  dev.lse = c->lse;
+  dev.s = c->s;
+  dev.q = c->q;
+  dev.q_equiv = c->qe;
+  dev.decision = c->dec;
+  dev.expected = c->expd;
+  dev.confidence = c->conf;
+  dev.mass = c->mass;
+  rc = score_sets_enqueue(c, c->stH, W, n_rows, c->st_row, c->st_tok, n_tok, c->st_co, n_cand, c->st_so,
+                          c->st_kind, n_sets, T, mode, dev_union, n_union, &dev, st);
+  if (rc != JET_OK) {
+    cudaStreamSynchronize(st);
+    return rc;
+  }
+  jet_set_out h;
+  std::memset(&h, 0, sizeof h);
+  if (out_host) h = *out_host;
+  auto D2H = [&](void* dst, const void* src, size_t bytes) {
+    if (e == cudaSuccess && dst && bytes) e = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToHost, st);
+  };
+  D2H(h.logp, c->logp, (size_t)n_tok * 4);
+  D2H(h.lse, c->lse, (size_t)n_rows * 4);
+  D2H(h.s, c->s, (size_t)n_cand * 4);
+  D2H(h.q, c->q, (size_t)n_cand * 4);
+  D2H(h.q_equiv, c->qe, (size_t)n_cand * 4);
+  D2H(h.decision, c->dec, (size_t)n_sets * 4);
+  D2H(h.expected, c->expd, (size_t)n_sets * 4);
+  D2H(h.confidence, c->conf, (size_t)n_sets * 4);
+  D2H(h.mass, c->mass, (size_t)n_sets * 4);
+  if (e != cudaSuccess) {
+    cudaStreamSynchronize(st);
+    return JET_ERR_CUDA;
+  }
+  return read_status(c, st);
+}
+
+}  // extern "C"

@@ -1,0 +1,125 @@
+// Internal declarations of libjetscore (GPU path).  Not part of the C ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "jetscore.h"
+
+namespace jet {
+
+// ---- full-vocabulary head tile shape (tcgen05, cta_group::1) ---------------
+constexpr int BM = 128;             // hidden rows per tile = TMEM lanes
+constexpr int BN = 256;             // vocabulary columns per tile = fp32 TMEM columns
+constexpr int BK = 64;              // bf16 elements per k-block = one 128-byte swizzle row
+constexpr int STAGES = 4;           // shared-memory pipeline depth
+constexpr int EPI_WARPS = 8;        // two warpgroups: column halves of a tile
+constexpr int HEAD_THREADS = (2 + EPI_WARPS) * 32;
+constexpr int A_STAGE_BYTES = BM * BK * 2;
+constexpr int B_STAGE_BYTES = BN * BK * 2;
+constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr int HEAD_SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int TMEM_COLS = 2 * BN;   // two accumulators (double buffer)
+
+// Device-side error word layout: err[0] = first status (0 = ok),
+// err[1] = index of the offending element, err[2] = where a wait gave up.
+constexpr int ERR_WORDS = 4;
+
+__device__ __forceinline__ void set_error(int* err, int code, int detail) {
+  if (atomicCAS(err, 0, code) == 0) err[1] = detail;
+}
+
+// Vocabulary-split schedule of the head: unit u = (row tile m, split s) covers
+// vocabulary tiles [s*n_vt/S, (s+1)*n_vt/S).  Units are ordered band by band
+// (Gm row tiles per band), split-major inside a band, so CTAs running together
+// share W tiles through L2 while the band's H tiles stay L2-resident.
+struct Plan {
+  int n_mt = 0, n_vt = 0, S = 1, Gm = 1, n_full_bands = 0, r_last = 0, units = 0, grid = 0;
+};
+
+struct HeadArgs {
+  int N, V, d;
+  Plan plan;
+  const int* row_ptr;   // [N+1]   CSR over rows of the scored tokens
+  const int2* row_list; // [n_tok] (token id, token index), sorted by id within a row
+  float* zg;            // [n_tok] gathered logit of each scored token
+  float2* part;         // [units*2*BM] per (unit, column half, row): (max, sum exp(z - max))
+  int* err;
+};
+
+// Decode unit u of the plan into (row tile, first vocab tile, end vocab tile).
+__host__ __device__ __forceinline__ void plan_unit(const Plan& p, int u, int& m, int& vt0, int& vt1) {
+  const int main_units = p.n_full_bands * p.Gm * p.S;
+  int split;
+  if (u < main_units) {
+    const int per_band = p.Gm * p.S;
+    const int band = u / per_band, w = u - band * per_band;
+    split = w / p.Gm;
+    m = band * p.Gm + (w - split * p.Gm);
+  } else {
+    const int w = u - main_units;
+    split = w / p.r_last;
+    m = p.n_full_bands * p.Gm + (w - split * p.r_last);
+  }
+  vt0 = (int)((int64_t)split * p.n_vt / p.S);
+  vt1 = (int)((int64_t)(split + 1) * p.n_vt / p.S);
+}
+
+// Unit index of (row tile m, split s): the inverse of plan_unit.
+__host__ __device__ __forceinline__ int plan_unit_of(const Plan& p, int m, int split) {
+  const int band = m / p.Gm;
+  if (band < p.n_full_bands) return band * p.Gm * p.S + split * p.Gm + (m - band * p.Gm);
+  return p.n_full_bands * p.Gm * p.S + split * p.r_last + (m - p.n_full_bands * p.Gm);
+}
+
+// ---- launchers (each returns cudaGetLastError() of its launch) -------------
+struct PrepArgs {
+  int n_rows, n_tok, V;
+  const int32_t* tok_row;   // NULL: token i is predicted by row i
+  const int32_t* tok_ids;
+  const int32_t* cand_offsets; int n_cand;   // NULL when no sets (jet_score_tokens)
+  const int32_t* set_offsets; const uint8_t* kind; int n_sets;
+  int mode; const int32_t* union_ids; int n_union;
+  int* row_ptr;    // [n_rows+1]
+  int* row_cur;    // [n_rows+1] scratch counters
+  int2* row_list;  // [n_tok]
+  int* upos;       // [n_tok] restricted mode: position of the token in the union
+  int* err;
+};
+cudaError_t launch_prep(const PrepArgs& a, cudaStream_t st);
+
+cudaError_t launch_head(const CUtensorMap& tmH, const CUtensorMap& tmW, const HeadArgs& a,
+                        cudaStream_t st);
+
+struct MergeArgs {
+  int N; Plan plan;
+  const float2* part; const float* zg;
+  const int* row_ptr; const int2* row_list;
+  float* lse;   // [N] or NULL
+  float* logp;  // [n_tok]
+  const int* err;
+};
+cudaError_t launch_merge(const MergeArgs& a, cudaStream_t st);
+
+struct RestrictedArgs {
+  int N, d, n_union;
+  const uint16_t* H; const uint16_t* W; const int32_t* union_ids;
+  const int* row_ptr; const int2* row_list; const int* upos;
+  float* lse; float* logp;
+  const int* err;
+};
+cudaError_t launch_restricted(const RestrictedArgs& a, cudaStream_t st);
+
+struct SetArgs {
+  int n_sets;
+  const float* logp; const int32_t* tok_ids; const int32_t* cand_offsets;
+  const int32_t* set_offsets; float T;
+  float* s; float* q; float* q_equiv; int32_t* decision; float* expected;
+  float* confidence; float* mass;
+  unsigned long long* hash;   // [n_cand] scratch
+  const int* err;
+};
+cudaError_t launch_sets(const SetArgs& a, cudaStream_t st);
+
+}  // namespace jet

@@ -1,0 +1,394 @@
+// Full-vocabulary scoring head on the 5th-generation tensor cores.
+//
+// For hidden rows H[N, d] and the output embedding W[V, d] (both bf16,
+// K-major) it computes, per row r and per vocabulary split of the schedule,
+//   m = max_v z[r, v],  s = sum_v exp(z[r, v] - m),     z = H W^T   (fp32)
+// and writes the logit z[r, tok] of every scored token whose id falls in the
+// split ("JET: Justification Evaluation in Transformer", Eq. 1-2: the
+// denominator runs over the full vocabulary; GPU scoring computes it but
+// transfers only the candidate log-probabilities).  The [N, V] logit matrix
+// lives only in tensor memory, one 128 x 256 fp32 tile at a time.
+//
+// Structure (one persistent CTA per SM, 320 threads):
+//   warp 0      TMA producer: H and W k-blocks (64 bf16 = 128 B, 128B swizzle)
+//               into a 4-stage shared-memory ring, completion on mbarriers;
+//   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators) and
+//               issues tcgen05.mma (M=128, N=256, K=16) from one thread;
+//   warps 2-9   epilogue: each thread owns one row (its TMEM lane) and half of
+//               the tile's columns, reads them with tcgen05.ld, folds them into
+//               a running (max, sum-exp) and picks out the logits of its row's
+//               tokens while walking the row's sorted token list.
+// The two accumulators let the epilogue of tile j overlap the MMAs of tile
+// j+1.  Every mbarrier wait is bounded: on timeout the kernel records
+// JET_ERR_TIMEOUT, drains its own copies and MMAs, frees TMEM and returns.
+#include <climits>
+
+#include "jet_internal.cuh"
+
+namespace jet {
+namespace {
+
+constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;   // 2 s per wait
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---- mbarrier ----------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for the phase of `bar` with the given parity.  Returns false if
+// another role asked to abort or if the wait exceeded WAIT_LIMIT_NS (then it
+// raises the abort flag and, when err is given, records where in err[2]).
+__device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err,
+                                       int where) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait(a, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(a, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > WAIT_LIMIT_NS) {
+        *abort_flag = 1;
+        if (err != nullptr && atomicCAS(err, 0, JET_ERR_TIMEOUT) == 0) err[2] = where;
+        return false;
+      }
+    }
+  }
+}
+
+// ---- TMA ----------------------------------------------------------------------
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+      : "memory");
+}
+
+// ---- tcgen05 ------------------------------------------------------------------
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes, 8-row swizzle atoms 1024 bytes apart (stride byte offset).
+__device__ __forceinline__ uint64_t sdesc_k128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);     // bits  0-13: start address >> 4
+  d |= (uint64_t)(16u >> 4) << 16;               // bits 16-29: leading byte offset (unused here)
+  d |= (uint64_t)(1024u >> 4) << 32;             // bits 32-45: stride byte offset >> 4
+  d |= (uint64_t)1 << 46;                        // bits 46-48: descriptor version 1
+  d |= (uint64_t)2 << 61;                        // bits 61-63: 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major,
+// N = BN, M = BM.
+constexpr uint32_t IDESC = (1u << 4)                 // D format: f32
+                           | (1u << 7)               // A format: bf16
+                           | (1u << 10)              // B format: bf16
+                           | ((uint32_t)(BN >> 3) << 17)
+                           | ((uint32_t)(BM >> 4) << 24);
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accum) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(IDESC), "r"(accum)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
+// Load 32 consecutive fp32 columns of this thread's TMEM lane, then wait for
+// the load.  The wait names the destination registers as operands so that no
+// use of them can be scheduled before it.
+__device__ __forceinline__ void tmem_ld32_wait(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+        "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile(
+      "tcgen05.wait::ld.sync.aligned;"
+      : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+        "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+        "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]),
+        "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]),
+        "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+      :
+      : "memory");
+}
+
+__device__ __forceinline__ float ex2(float x) {   // hardware 2^x (MUFU), flushes subnormals
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+constexpr float LOG2E = 1.4426950408889634f;
+
+__global__ void __launch_bounds__(HEAD_THREADS, 1)
+    head_lse_gather_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmW,
+                           const HeadArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  // 128B-swizzled operand tiles must start on 1024-byte boundaries
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * B_STAGE_BYTES);
+  uint64_t* full = bars;                  // [STAGES] TMA -> MMA
+  uint64_t* empty = bars + STAGES;        // [STAGES] MMA -> TMA
+  uint64_t* tfull = bars + 2 * STAGES;    // [2] MMA -> epilogue
+  uint64_t* tempty = tfull + 2;           // [2] epilogue -> MMA
+  uint64_t* drain = tempty + 2;           // [1] MMA drain on abort
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (*(volatile const int*)a.err != 0) return;   // pre-pass rejected the batch (uniform)
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], EPI_WARPS);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const Plan& P = a.plan;
+  const int kblocks = a.d / BK;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_mask = 0, issued_parity = 0;   // per stage: has a load, parity of its phase
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < P.units; u += gridDim.x) {
+        int m, vt0, vt1;
+        plan_unit(P, u, m, vt0, vt1);
+        for (int vt = vt0; ok && vt < vt1; ++vt) {
+          if (*abort_flag) { ok = false; break; }
+          for (int kb = 0; kb < kblocks; ++kb) {
+            if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.err, 1)) { ok = false; break; }
+            mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+            tma_load_2d(sA + stage * A_STAGE_BYTES, &tmH, kb * BK, m * BM, &full[stage]);
+            tma_load_2d(sB + stage * B_STAGE_BYTES, &tmW, kb * BK, vt * BN, &full[stage]);
+            issued_mask |= 1u << stage;
+            issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          }
+        }
+      }
+      if (ok) {
+        // tail: wait until the MMA has released every stage, so that no
+        // barrier arrival is still pending when the CTA exits
+        for (int i = 0; i < STAGES; ++i) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.err, 5)) break;
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      } else {
+        // abort: let copies already in flight land before the CTA exits
+        volatile int never = 0;
+        for (int s = 0; s < STAGES; ++s)
+          if (issued_mask & (1u << s)) mbar_wait(&full[s], (issued_parity >> s) & 1u, &never, nullptr, 0);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true, any = false;
+      for (int u = blockIdx.x; ok && u < P.units; u += gridDim.x) {
+        int m, vt0, vt1;
+        plan_unit(P, u, m, vt0, vt1);
+        for (int vt = vt0; ok && vt < vt1; ++vt) {
+          if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, a.err, 2)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+          for (int kb = 0; kb < kblocks; ++kb) {
+            if (!mbar_wait(&full[stage], phase, abort_flag, a.err, 3)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t a0 = smem_u32(sA + stage * A_STAGE_BYTES);
+            const uint32_t b0 = smem_u32(sB + stage * B_STAGE_BYTES);
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k)   // 16 bf16 = 32 bytes along K per MMA
+              tc_mma(d_tmem, sdesc_k128(a0 + 32 * k), sdesc_k128(b0 + 32 * k), (kb | k) != 0);
+            tc_commit(&empty[stage]);
+            any = true;
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          }
+          if (!ok) break;
+          tc_commit(&tfull[acc]);
+          acc ^= 1;
+          if (acc == 0) acc_phase ^= 1u;
+        }
+      }
+      if (!ok && any) {   // wait until every MMA issued so far has completed
+        volatile int never = 0;
+        tc_commit(drain);
+        mbar_wait(drain, 0, &never, nullptr, 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;              // TMEM lanes this warp may access
+    const int half = (warp - 2) >> 2;          // column half of each tile
+    const int row_in_tile = quarter * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < P.units; u += gridDim.x) {
+      int m, vt0, vt1;
+      plan_unit(P, u, m, vt0, vt1);
+      const int row = m * BM + row_in_tile;
+      const bool valid = row < a.N;
+      int e = 0, e_end = 0, t_next = INT_MAX;
+      if (valid) {
+        e = a.row_ptr[row];
+        e_end = a.row_ptr[row + 1];
+        const int col_begin = vt0 * BN;
+        while (e < e_end && a.row_list[e].x < col_begin) ++e;
+        if (e < e_end) t_next = a.row_list[e].x;
+      }
+      float m_run = -INFINITY, s_run = 0.f;
+      for (int vt = vt0; vt < vt1; ++vt) {
+        if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, a.err, 4)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN + half * 128);
+        const int col0 = vt * BN + half * 128;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          __syncwarp();                            // .sync.aligned: whole warp, converged
+          tmem_ld32_wait(taddr + 32 * c, r);
+          float x[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(r[i]);
+          const int cb = col0 + 32 * c;
+          if (cb + 32 > a.V) {                    // vocabulary tail: columns >= V do not exist
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (cb + i >= a.V) x[i] = -INFINITY;
+          }
+          while (t_next < cb + 32) {               // this row's tokens in this chunk
+            if (t_next >= cb) {
+              const int kk = t_next - cb;
+              float g = 0.f;
+#pragma unroll
+              for (int i = 0; i < 32; ++i) g = (i == kk) ? x[i] : g;
+              a.zg[a.row_list[e].y] = g;
+            }
+            ++e;
+            t_next = (e < e_end) ? a.row_list[e].x : INT_MAX;
+          }
+          float cmax = x[0];
+#pragma unroll
+          for (int i = 1; i < 32; ++i) cmax = fmaxf(cmax, x[i]);
+          const float m_new = fmaxf(m_run, cmax);
+          if (m_new != -INFINITY) {
+            const float mb = m_new * LOG2E;
+            float cs = 0.f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) cs += ex2(fmaf(x[i], LOG2E, -mb));
+            s_run = s_run * ex2((m_run - m_new) * LOG2E) + cs;
+            m_run = m_new;
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      if (ok && valid) a.part[((size_t)u * 2 + half) * BM + row_in_tile] = make_float2(m_run, s_run);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_head(const CUtensorMap& tmH, const CUtensorMap& tmW, const HeadArgs& a, cudaStream_t st) {
+  static bool configured = false;   // per process; the attribute is per function
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(head_lse_gather_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         HEAD_SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  head_lse_gather_kernel<<<a.plan.grid, HEAD_THREADS, HEAD_SMEM_BYTES, st>>>(tmH, tmW, a);
+  return cudaGetLastError();
+}
+
+}  // namespace jet

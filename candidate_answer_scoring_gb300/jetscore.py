@@ -1,0 +1,234 @@
+"""Thin ctypes binding of libjetscore (argument marshalling only).
+
+Every step of the scoring head runs in the library's CUDA kernels; this module
+only passes torch tensors' device pointers, sizes and the current CUDA stream
+through the C ABI declared in ``include/jetscore.h``.  It has no CPU path: if
+the library is not built, loading it raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from typing import Dict, Optional, Sequence
+
+import torch
+
+from . import build as _build
+
+JET_OK = 0
+JET_ERR_ARG = -1
+JET_ERR_TOKEN_RANGE = -2
+JET_ERR_OFFSETS = -3
+JET_ERR_MODE = -4
+JET_ERR_NOT_IN_UNION = -5
+JET_ERR_WORKSPACE = -6
+JET_ERR_UNSUPPORTED = -7
+JET_ERR_CUDA = -8
+JET_ERR_TIMEOUT = -9
+
+JET_KIND_CHOICE, JET_KIND_BINARY, JET_KIND_ORDINAL = 0, 1, 2
+JET_MODE_FULL, JET_MODE_RESTRICTED = 0, 1
+JET_MAX_UNION = 4096
+
+SET_OUTPUTS = ("logp", "lse", "s", "q", "q_equiv", "decision", "expected", "confidence", "mass")
+
+
+class JetError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+class _SetOut(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in SET_OUTPUTS]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load() -> C.CDLL:
+    """Load the in-tree libjetscore.so; raise if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"libjetscore is not built ({path} missing); run "
+                           "candidate_answer_scoring_gb300.build.build() with the CUDA toolkit")
+    lib = C.CDLL(path)
+    P, I, F = C.c_void_p, C.c_int, C.c_float
+    lib.jet_create.argtypes = [C.POINTER(P), I, I, I, I, I]
+    lib.jet_destroy.argtypes = [P]
+    lib.jet_destroy.restype = None
+    lib.jet_status_string.argtypes = [I]
+    lib.jet_status_string.restype = C.c_char_p
+    lib.jet_score_tokens.argtypes = [P, P, P, P, I, P, P, P]
+    sets_sig = [P, P, P, I, P, P, I, P, I, P, P, I, F, I, P, I, C.POINTER(_SetOut), P]
+    for name in ("jet_score_sets", "jet_score_sets_async", "jet_score_sets_host"):
+        getattr(lib, name).argtypes = sets_sig
+    lib.jet_sync_status.argtypes = [P, P]
+    lib.jet_plan_info.argtypes = [P, I, C.POINTER(C.c_int)]
+    lib.jet_profile_enable.argtypes = [P, I]
+    lib.jet_profile_read.argtypes = [P, C.POINTER(C.c_double), I]
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().jet_status_string(int(status)).decode()
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _stream(device: torch.device):
+    return C.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _check_dev(t: torch.Tensor, name: str, device: torch.device, dtypes: Sequence[torch.dtype]):
+    if not isinstance(t, torch.Tensor) or t.device != device:
+        raise ValueError(f"{name} must be a tensor on {device}")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+_BF16 = (torch.bfloat16, torch.int16, torch.uint16)
+
+
+class JetScorer:
+    """A libjetscore context: output embedding shape [V, d] and a workspace for
+    up to ``max_rows`` hidden rows and ``max_tokens`` scored tokens per call."""
+
+    def __init__(self, d: int, V: int, max_rows: int, max_tokens: int, device: int = 0):
+        self.lib = load()
+        self.d, self.V, self.max_rows, self.max_tokens = d, V, max_rows, max_tokens
+        self.device = torch.device("cuda", device)
+        h = C.c_void_p()
+        rc = self.lib.jet_create(C.byref(h), d, V, max_rows, max_tokens, device)
+        if rc != JET_OK:
+            raise JetError(rc, "jet_create")
+        self._h = h
+
+    def close(self) -> None:
+        if getattr(self, "_h", None):
+            self.lib.jet_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # -------------------------------------------------------------- calls
+    def plan_info(self, n_rows: int) -> Dict[str, int]:
+        out = (C.c_int * 8)()
+        rc = self.lib.jet_plan_info(self._h, int(n_rows), out)
+        if rc != JET_OK:
+            raise JetError(rc, "jet_plan_info")
+        keys = ("row_tiles", "vocab_tiles", "splits", "band_height", "units", "ctas", "tile_rows", "tile_cols")
+        return dict(zip(keys, list(out)))
+
+    def score_tokens(self, H: torch.Tensor, W: torch.Tensor, tok_ids: torch.Tensor, want_lse: bool = False):
+        """logp[i] = log softmax_V(H[i] W^T)[tok_ids[i]] (and lse[i])."""
+        dev = self.device
+        _check_dev(H, "H", dev, _BF16); _check_dev(W, "W", dev, _BF16)
+        _check_dev(tok_ids, "tok_ids", dev, (torch.int32,))
+        n = tok_ids.numel()
+        logp = torch.empty(n, dtype=torch.float32, device=dev)
+        lse = torch.empty(n, dtype=torch.float32, device=dev) if want_lse else None
+        rc = self.lib.jet_score_tokens(self._h, _ptr(H), _ptr(W), _ptr(tok_ids), n, _ptr(logp), _ptr(lse),
+                                       _stream(dev))
+        if rc != JET_OK:
+            raise JetError(rc, "jet_score_tokens")
+        return (logp, lse) if want_lse else logp
+
+    def alloc_outputs(self, n_rows: int, n_tok: int, n_cand: int, n_sets: int,
+                      want: Sequence[str] = SET_OUTPUTS) -> Dict[str, torch.Tensor]:
+        dev = self.device
+        sizes = dict(logp=n_tok, lse=n_rows, s=n_cand, q=n_cand, q_equiv=n_cand, decision=n_sets,
+                     expected=n_sets, confidence=n_sets, mass=n_sets)
+        return {k: torch.empty(sizes[k], dtype=torch.int32 if k == "decision" else torch.float32, device=dev)
+                for k in want}
+
+    def _set_args(self, H, W, tok_row, tok_ids, cand_offsets, set_offsets, kind, T, mode, union_ids, out):
+        so = _SetOut(*[_ptr(out.get(n)) for n in SET_OUTPUTS])
+        n_union = 0 if union_ids is None else union_ids.numel()
+        args = [self._h, _ptr(H), _ptr(W), H.shape[0], _ptr(tok_row), _ptr(tok_ids), tok_ids.numel(),
+                _ptr(cand_offsets), cand_offsets.numel() - 1, _ptr(set_offsets), _ptr(kind),
+                set_offsets.numel() - 1, C.c_float(T), int(mode), _ptr(union_ids), n_union, C.byref(so)]
+        return args, so
+
+    def score_sets(self, H, W, tok_row, tok_ids, cand_offsets, set_offsets, kind, T: float,
+                   mode: int = JET_MODE_FULL, union_ids=None, out: Optional[Dict[str, torch.Tensor]] = None,
+                   sync: bool = True) -> Dict[str, torch.Tensor]:
+        """Whole scoring head on device tensors; returns the output tensors."""
+        dev = self.device
+        _check_dev(H, "H", dev, _BF16); _check_dev(W, "W", dev, _BF16)
+        for name, t in (("tok_row", tok_row), ("tok_ids", tok_ids), ("cand_offsets", cand_offsets),
+                        ("set_offsets", set_offsets)):
+            _check_dev(t, name, dev, (torch.int32,))
+        _check_dev(kind, "kind", dev, (torch.uint8,))
+        if union_ids is not None:
+            _check_dev(union_ids, "union_ids", dev, (torch.int32,))
+        if out is None:
+            out = self.alloc_outputs(H.shape[0], tok_ids.numel(), cand_offsets.numel() - 1,
+                                     set_offsets.numel() - 1)
+        args, keep = self._set_args(H, W, tok_row, tok_ids, cand_offsets, set_offsets, kind, T, mode, union_ids,
+                                    out)
+        fn = self.lib.jet_score_sets if sync else self.lib.jet_score_sets_async
+        rc = fn(*args, _stream(dev))
+        if rc != JET_OK:
+            raise JetError(rc, "jet_score_sets")
+        return out
+
+    KERNELS = ("prep", "head", "merge", "restricted", "sets")
+
+    def profile(self, enable: bool) -> None:
+        rc = self.lib.jet_profile_enable(self._h, 1 if enable else 0)
+        if rc != JET_OK:
+            raise JetError(rc, "jet_profile_enable")
+
+    def profile_read(self) -> Dict[str, Dict[str, float]]:
+        """Per kernel kind: launches and total device milliseconds since the last read."""
+        out = (C.c_double * 11)()
+        rc = self.lib.jet_profile_read(self._h, out, 11)
+        if rc != JET_OK:
+            raise JetError(rc, "jet_profile_read")
+        res = {k: {"launches": int(out[2 * i]), "ms": float(out[2 * i + 1])} for i, k in enumerate(self.KERNELS)}
+        res["untimed_launches"] = int(out[10])
+        return res
+
+    def sync_status(self) -> int:
+        return self.lib.jet_sync_status(self._h, _stream(self.device))
+
+    def score_sets_host(self, H, W, tok_row, tok_ids, cand_offsets, set_offsets, kind, T: float,
+                        mode: int = JET_MODE_FULL, union_ids=None,
+                        out: Optional[Dict[str, torch.Tensor]] = None) -> Dict[str, torch.Tensor]:
+        """End-to-end call with HOST (CPU, ideally pinned) tensors; W stays on the device."""
+        _check_dev(W, "W", self.device, _BF16)
+        cpu = torch.device("cpu")
+        _check_dev(H, "H", cpu, _BF16)
+        for name, t in (("tok_row", tok_row), ("tok_ids", tok_ids), ("cand_offsets", cand_offsets),
+                        ("set_offsets", set_offsets)):
+            _check_dev(t, name, cpu, (torch.int32,))
+        _check_dev(kind, "kind", cpu, (torch.uint8,))
+        if out is None:
+            n = (H.shape[0], tok_ids.numel(), cand_offsets.numel() - 1, set_offsets.numel() - 1)
+            sizes = dict(logp=n[1], lse=n[0], s=n[2], q=n[2], q_equiv=n[2], decision=n[3], expected=n[3],
+                         confidence=n[3], mass=n[3])
+            out = {k: torch.empty(v, dtype=torch.int32 if k == "decision" else torch.float32).pin_memory()
+                   for k, v in sizes.items()}
+        args, keep = self._set_args(H, W, tok_row, tok_ids, cand_offsets, set_offsets, kind, T, mode, union_ids,
+                                    out)
+        rc = self.lib.jet_score_sets_host(*args, _stream(self.device))
+        if rc != JET_OK:
+            raise JetError(rc, "jet_score_sets_host")
+        return out

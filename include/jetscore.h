@@ -1,0 +1,206 @@
+/*
+ * jetscore.h -- C ABI of libjetscore, the candidate-set scoring head on one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * What it computes (method: "JET: Justification Evaluation in Transformer";
+ * contracts: Gemma/MLX architecture page, "Candidate likelihoods" and "Output
+ * contracts"; restricted head: PARALLEL_SCORING page, "Execution" steps 5-6):
+ *
+ *   z[r, v]  = H[r, :] . W[v, :]                       logits of hidden row r
+ *   lse[r]   = log sum_v exp z[r, v]                   full-vocabulary denominator (JET Eq. 1)
+ *   l_j      = z[tok_row_j, tok_ids_j] - lse[tok_row_j]                        (JET Eq. 2)
+ *   s(c)     = sum over the candidate's tokens of l    sequence log-likelihood  (JET Eq. 3)
+ *   q(c)     = exp(s(c)/T) / sum_{c' in set} exp(s(c')/T)                       (JET Eq. 4)
+ *   decision = first index of max s (fixed-order tie-break)                    (JET Eq. 5)
+ *   expected = sum_i i q_i  (binary {false,true}: = q(true); ordinal: level mean)
+ *   confidence = 1 - H(q)/ln K;  mass = sum of exp(s) at T=1 over distinct token
+ *   sequences (allowed_token_mass);  q_equiv(c) = q summed over candidates with
+ *   c's token sequence (labels with identical text).
+ *
+ * The [N, V] logit matrix is never written to memory: the projection, the
+ * running max / sum-exp over vocabulary tiles and the gather of the supplied
+ * token's logit happen in one kernel.
+ *
+ * Conventions shared by every call:
+ *   - All array arguments are DEVICE pointers on the context's device, except
+ *     in jet_score_sets_host, where they are HOST pointers.  The caller owns
+ *     every input and output buffer; the library never frees or retains them.
+ *   - H is bf16 row-major [n_rows, d]; W is bf16 row-major [V, d] (the output
+ *     embedding / tied input embedding).  Both base addresses must be 16-byte
+ *     aligned.  d must be a multiple of 64, 64 <= d <= 16384; 1 <= V < 2^31.
+ *   - Index arrays are int32; kind is uint8; outputs are fp32 (decision int32).
+ *   - Calls are stream-ordered on `cuda_stream` (a cudaStream_t, or NULL for
+ *     the legacy default stream).  A context serves one stream at a time and
+ *     is not thread-safe.
+ *   - Return value: JET_OK or a negative status.  Host checks (sizes, T,
+ *     mode, alignment) fail before anything is launched.  Index checks run in
+ *     a device pre-pass that writes an error word; the synchronous calls wait
+ *     for the stream once at the end and return that word.  On any error the
+ *     outputs are unspecified.  Nothing in the library traps or asserts on the
+ *     device; every device-side wait is bounded and reports JET_ERR_TIMEOUT.
+ */
+#ifndef JETSCORE_H
+#define JETSCORE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct jet_ctx jet_ctx; /* opaque: device workspace + schedule cache */
+
+enum {
+  JET_OK = 0,
+  JET_ERR_ARG = -1,          /* bad size, pointer, alignment, T, kind value, or context */
+  JET_ERR_TOKEN_RANGE = -2,  /* a token id outside [0, V) or a row outside [0, n_rows) */
+  JET_ERR_OFFSETS = -3,      /* CSR offsets not monotone / not covering, empty candidate
+                                or set, binary set with K != 2, ordinal set with K < 2 */
+  JET_ERR_MODE = -4,         /* mode not FULL/RESTRICTED, or restricted-mode candidate
+                                longer than one token */
+  JET_ERR_NOT_IN_UNION = -5, /* restricted mode: candidate token not in union_ids, or a
+                                union id repeated */
+  JET_ERR_WORKSPACE = -6,    /* n_rows / n_tok beyond the sizes given to jet_create */
+  JET_ERR_UNSUPPORTED = -7,  /* device is not sm_103 (GB300) or lacks the features used */
+  JET_ERR_CUDA = -8,         /* a CUDA runtime call failed */
+  JET_ERR_TIMEOUT = -9       /* a bounded device-side wait gave up (kernel returned early) */
+};
+
+enum { JET_KIND_CHOICE = 0, JET_KIND_BINARY = 1, JET_KIND_ORDINAL = 2 };
+enum { JET_MODE_FULL = 0, JET_MODE_RESTRICTED = 1 };
+
+#define JET_MAX_UNION 4096 /* restricted mode: largest accepted union */
+
+/*
+ * jet_create: make a context on CUDA device `device` for an output embedding of
+ * shape [V, d], and allocate its device workspace for up to `max_rows` hidden
+ * rows and `max_tokens` scored tokens per call (candidates and sets are bounded
+ * by max_tokens as every candidate has >= 1 token).  Also allocates device
+ * staging buffers of that size for jet_score_sets_host.
+ * Errors: JET_ERR_ARG (sizes), JET_ERR_UNSUPPORTED (not sm_103), JET_ERR_CUDA.
+ * On success *out owns the workspace until jet_destroy.
+ */
+int jet_create(jet_ctx **out, int d, int V, int max_rows, int max_tokens, int device);
+
+/* Free the context and its workspace (waits for the device).  NULL is a no-op. */
+void jet_destroy(jet_ctx *ctx);
+
+/* Static, human-readable text for a status code. */
+const char *jet_status_string(int status);
+
+/*
+ * jet_score_tokens: one scored token per hidden row (JET Eq. 1-2, the
+ * per-position log-probability of a supplied token under teacher forcing):
+ *   logp[i] = z[i, tok_ids[i]] - lse[i],   0 <= i < n_pos.
+ * H [n_pos, d] bf16; W [V, d] bf16; tok_ids [n_pos] int32.
+ * logp [n_pos] fp32 (required); lse [n_pos] fp32 or NULL.
+ * n_pos == 0 returns JET_OK without launching.  Synchronous.
+ */
+int jet_score_tokens(jet_ctx *ctx, const void *H_bf16, const void *W_bf16, const int32_t *tok_ids,
+                     int n_pos, float *logp, float *lse, void *cuda_stream);
+
+/* Caller-owned device output buffers of jet_score_sets; NULL = not wanted. */
+typedef struct {
+  float *logp;       /* [n_tok]  l_j (full vocabulary) or z - lse over the union (restricted) */
+  float *lse;        /* [n_rows] per-row log-sum-exp over the normaliser set */
+  float *s;          /* [n_cand] sequence log-likelihood s(c) */
+  float *q;          /* [n_cand] q(c) = softmax over the set of s/T */
+  float *q_equiv;    /* [n_cand] q summed over candidates with an identical token sequence */
+  int32_t *decision; /* [n_sets] index within the set of the first maximum of s */
+  float *expected;   /* [n_sets] sum_i i q_i (binary sets: q(true)) */
+  float *confidence; /* [n_sets] 1 - H(q)/ln K (K = 1: 1) */
+  float *mass;       /* [n_sets] sum of exp(s) at T = 1 over distinct token sequences */
+} jet_set_out;
+
+/*
+ * jet_score_sets: the whole scoring head for a batch of candidate sets.
+ * Layout (CSR):
+ *   H [n_rows, d] bf16 -- final hidden state at each teacher-forced position
+ *       (JET, candidate evaluation under teacher forcing; Gemma/MLX page: one
+ *       vocabulary vector per field for single-token candidates, one row per
+ *       predicted token for multi-token candidates).  A row may serve several
+ *       tokens.
+ *   tok_row[n_tok], tok_ids[n_tok] -- for scored token j, the row predicting it
+ *       and its id; a candidate's tokens are contiguous and in order.
+ *   cand_offsets[n_cand+1] -- tokens of candidate c are [cand_offsets[c],
+ *       cand_offsets[c+1]); cand_offsets[0] = 0, cand_offsets[n_cand] = n_tok.
+ *   set_offsets[n_sets+1] -- candidates of set k, same convention over n_cand.
+ *   kind[n_sets] -- JET_KIND_*: binary sets have K = 2 in order {false, true};
+ *       ordinal sets K >= 2 levels in order; choice sets K >= 1.
+ *   T > 0, finite -- temperature applied once to s before the set softmax
+ *       (PARALLEL_SCORING page, "V2 probability default"); l, s, decision and
+ *       mass do not depend on it.
+ *   mode -- JET_MODE_FULL: normalise over the full vocabulary.
+ *       JET_MODE_RESTRICTED: normalise over union_ids[n_union] (distinct ids,
+ *       1 <= n_union <= JET_MAX_UNION); every candidate is one token of the
+ *       union (PARALLEL_SCORING page, "Execution" step 5).  union_ids is ignored
+ *       in full mode.
+ * out -- host struct of device pointers; any member may be NULL.
+ * Empty batches (n_tok == 0 with n_cand == n_sets == 0) return JET_OK.
+ * Synchronous: waits for `cuda_stream` once, then returns the device status.
+ */
+int jet_score_sets(jet_ctx *ctx, const void *H_bf16, const void *W_bf16, int n_rows,
+                   const int32_t *tok_row, const int32_t *tok_ids, int n_tok,
+                   const int32_t *cand_offsets, int n_cand, const int32_t *set_offsets,
+                   const uint8_t *kind, int n_sets, float T, int mode, const int32_t *union_ids,
+                   int n_union, const jet_set_out *out, void *cuda_stream);
+
+/*
+ * jet_score_sets_async: as jet_score_sets but returns after enqueueing (host
+ * checks only).  The device status of the last enqueued call is returned by
+ * jet_sync_status, which waits for `cuda_stream`.  For benchmarking and
+ * pipelining; results are valid once the stream has reached them.
+ */
+int jet_score_sets_async(jet_ctx *ctx, const void *H_bf16, const void *W_bf16, int n_rows,
+                         const int32_t *tok_row, const int32_t *tok_ids, int n_tok,
+                         const int32_t *cand_offsets, int n_cand, const int32_t *set_offsets,
+                         const uint8_t *kind, int n_sets, float T, int mode,
+                         const int32_t *union_ids, int n_union, const jet_set_out *out,
+                         void *cuda_stream);
+int jet_sync_status(jet_ctx *ctx, void *cuda_stream);
+
+/*
+ * jet_score_sets_host: end-to-end entry for callers holding HOST buffers.
+ * W_bf16 is a DEVICE pointer (the output embedding stays resident, like any
+ * model weight); every other array (H, the index arrays, union_ids, and the
+ * members of *out_host) is a HOST pointer (pinned memory gives full copy
+ * speed; pageable memory works).  The call copies the inputs into the
+ * context's device staging buffers, runs jet_score_sets on them, copies the
+ * requested outputs back and waits for `cuda_stream`.
+ * Errors: as jet_score_sets.
+ */
+int jet_score_sets_host(jet_ctx *ctx, const void *H_bf16_host, const void *W_bf16_dev, int n_rows,
+                        const int32_t *tok_row, const int32_t *tok_ids, int n_tok,
+                        const int32_t *cand_offsets, int n_cand, const int32_t *set_offsets,
+                        const uint8_t *kind, int n_sets, float T, int mode,
+                        const int32_t *union_ids, int n_union, const jet_set_out *out_host,
+                        void *cuda_stream);
+
+/*
+ * jet_plan_info: the vocabulary-split schedule the full-vocabulary head uses
+ * for `n_rows` rows (for reports and tests).  info[0..7] receive:
+ *   row tiles, vocabulary tiles, splits per row tile, band height (row tiles
+ *   whose units run together), units, CTAs launched, rows per tile, vocabulary
+ *   columns per tile.
+ * Returns JET_ERR_ARG for a NULL pointer or n_rows outside [1, max_rows].
+ */
+int jet_plan_info(jet_ctx *ctx, int n_rows, int *info8);
+
+/*
+ * Kernel timing.  jet_profile_enable(ctx, 1) makes the library record a CUDA
+ * event pair on the launching stream around each of its kernel launches (no
+ * extra synchronisation).  jet_profile_read waits for the recorded events and
+ * writes, for kernel kind k in {0 pre-pass, 1 full-vocabulary head, 2 split
+ * merge, 3 restricted head, 4 set rules}: out[2k] = launches, out[2k+1] =
+ * total milliseconds; then clears the record.  n_out must be >= 10.  Up to
+ * 65536 launches per kind are timed between reads; later ones are counted
+ * only (out[2k] counts all, out[10] = launches that were not timed).
+ */
+int jet_profile_enable(jet_ctx *ctx, int enable);
+int jet_profile_read(jet_ctx *ctx, double *out, int n_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* JETSCORE_H */

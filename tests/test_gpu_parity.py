@@ -1,0 +1,259 @@
+"""GPU parity: the CUDA path against the fp64 oracle on the same seeded inputs,
+through the C ABI (via the thin ctypes binding).
+
+Small and mid-size cases are compared element by element; they span several
+row and vocabulary tiles with ragged tails.  The five named workloads run at
+full size in the launch configuration the benchmark times, and are compared
+on sampled sets (the oracle computes only those) plus properties that hold at
+any size.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wk
+from parity import check_duplicates, compare, subset
+
+pytestmark = pytest.mark.gpu
+
+OUT_KEYS = ("logp", "lse", "s", "q", "q_equiv", "decision", "expected", "confidence", "mass")
+
+
+@pytest.fixture(scope="module")
+def jet():
+    import candidate_answer_scoring_gb300 as jet
+    jet.load()
+    return jet
+
+
+def to_dev(wl, dev="cuda:0"):
+    t = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).to(dev).view(dt) if dt is torch.bfloat16 \
+        else torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    d = dict(H=t(wl.H.view(np.int16), torch.bfloat16), W=t(wl.W.view(np.int16), torch.bfloat16),
+             tok_row=t(wl.tok_row, None), tok_ids=t(wl.tok_ids, None), cand_offsets=t(wl.cand_offsets, None),
+             set_offsets=t(wl.set_offsets, None), kind=t(wl.kind, None))
+    d["union_ids"] = None if wl.union_ids is None else t(wl.union_ids, None)
+    return d
+
+
+def run_gpu(jet, wl, scorer=None, dev_inputs=None):
+    if scorer is None:
+        scorer = jet.JetScorer(wl.d, wl.V, max(1, wl.N), max(1, wl.n_tok))
+    x = dev_inputs if dev_inputs is not None else to_dev(wl)
+    out = scorer.score_sets(x["H"], x["W"], x["tok_row"], x["tok_ids"], x["cand_offsets"], x["set_offsets"],
+                            x["kind"], wl.T, wl.mode, x["union_ids"])
+    torch.cuda.synchronize()
+    return {k: v.cpu().numpy() for k, v in out.items()}
+
+
+# ---------------------------------------------------------------------------
+# element-by-element parity on small / mid-size cases
+# ---------------------------------------------------------------------------
+def test_tiny_workload(jet):
+    wl = wk.tiny()
+    gpu = run_gpu(jet, wl)
+    orc = oracle.score_workload(wl)
+    compare(wl, gpu, orc)
+    assert check_duplicates(wl, gpu) >= 1
+
+
+CASES = {
+    # name: (d, V, n_sets, kwargs)
+    "ragged-rows-and-vocab": (128, 1000, 40, dict(K=(2, 8), length=(1, 6))),
+    "shared-rows-multitile": (256, 3000, 60, dict(K=(2, 10), length=(1, 5), row_mode="per_key")),
+    "peaked-temperature": (192, 2051, 30, dict(K=(2, 12), length=(1, 8), peak=(0.9, 0.99), T=wk.T_FITTED)),
+    "vocab-below-one-tile": (64, 7, 25, dict(K=(2, 5), length=(1, 3), dup_prob=0.3)),
+    "vocab-exact-tiles": (64, 2048, 50, dict(K=(1, 6), length=(1, 4), kinds=(0,))),
+    "long-k": (128, 1500, 6, dict(K=(60, 70), length=(1, 3), kinds=(0,))),
+}
+
+
+@pytest.mark.parametrize("case", sorted(CASES))
+def test_custom_parity(jet, case):
+    d, V, n_sets, kw = CASES[case]
+    wl = wk.custom(d, V, n_sets, seed=hash(case) % 1000, **kw)
+    gpu = run_gpu(jet, wl)
+    orc = oracle.score_workload(wl)
+    compare(wl, gpu, orc)
+    check_duplicates(wl, gpu)
+
+
+def test_score_tokens(jet):
+    rng = np.random.default_rng(0)
+    d, V, n = 128, 5000, 700
+    W = wk.gen_W(99, V, d)
+    H = wk.to_bf16_bits(rng.normal(size=(n, d)).astype(np.float32))
+    tok = rng.integers(0, V, size=n).astype(np.int32)
+    sc = jet.JetScorer(d, V, n, n)
+    Hd = torch.from_numpy(H.view(np.int16)).cuda().view(torch.bfloat16)
+    Wd = torch.from_numpy(W.view(np.int16)).cuda().view(torch.bfloat16)
+    logp, lse = sc.score_tokens(Hd, Wd, torch.from_numpy(tok).cuda(), want_lse=True)
+    ref_lp, ref_lse = oracle.score_tokens(H, W, np.arange(n, dtype=np.int32), tok)
+    assert np.abs(logp.cpu().numpy() - ref_lp).max() <= 2e-3
+    assert np.abs(lse.cpu().numpy() - ref_lse).max() <= 2e-3
+
+
+def test_restricted_parity(jet):
+    base = wk.binary_batch(n_questions=40, random_pairs=True, d=128, V=3000)
+    wl = wk.binary_restricted(base=base)
+    gpu = run_gpu(jet, wl)
+    orc = oracle.score_workload(wl)
+    compare(wl, gpu, orc)
+
+
+def test_restricted_union_larger_than_one_chunk(jet):
+    """Single-token sets over a 600-code union, d=1024: the union is staged in
+    several shared-memory chunks; rows shared by all codes of a set."""
+    rng = np.random.default_rng(5)
+    d, V = 1024, 20000
+    union = rng.choice(V, size=600, replace=False).astype(np.int32)
+    sets = []
+    for _ in range(50):
+        K = int(rng.integers(2, 9))
+        sets.append(wk._SetSpec(wk.KIND_CHOICE, [(int(t),) for t in rng.choice(union, size=K, replace=False)]))
+    W = wk.gen_W(1234, V, d)
+    wl = wk._build("restricted-600", 1234, d, V, W, sets, 1.5, row_mode="per_key")
+    wl = wl.with_mode(wk.MODE_RESTRICTED, 1.5, union)
+    gpu = run_gpu(jet, wl)
+    orc = oracle.score_workload(wl)
+    compare(wl, gpu, orc)
+
+
+def test_full_equals_restricted_when_union_is_vocab(jet):
+    base = wk.binary_batch(n_questions=30, random_pairs=True, d=64, V=1500)
+    full = run_gpu(jet, base)
+    rest = run_gpu(jet, base.with_mode(wk.MODE_RESTRICTED, base.T, np.arange(1500, dtype=np.int32)))
+    for k in ("logp", "s", "q", "expected", "confidence", "mass"):
+        np.testing.assert_allclose(rest[k], full[k], atol=2e-5, rtol=1e-4)
+    np.testing.assert_array_equal(rest["decision"], full["decision"])
+
+
+def test_edge_cases(jet):
+    # one row, one single-token candidate (K = 1)
+    wl = wk.custom(64, 300, 1, K=(1, 1), length=(1, 1), kinds=(0,), seed=3)
+    gpu = run_gpu(jet, wl)
+    orc = oracle.score_workload(wl)
+    compare(wl, gpu, orc)
+    assert gpu["q"][0] == 1.0 and gpu["decision"][0] == 0 and gpu["confidence"][0] == 1.0
+    # empty batch: nothing launched, status ok
+    sc = jet.JetScorer(64, 300, 4, 4)
+    x = to_dev(wl)
+    e = torch.empty(0, dtype=torch.int32, device="cuda")
+    z = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sc.score_sets(x["H"], x["W"], e, e, z, z, torch.empty(0, dtype=torch.uint8, device="cuda"), 1.0,
+                  out={k: torch.empty(1, device="cuda") for k in ("s",)})
+    # batch exactly at the workspace limit
+    wl = wk.custom(64, 500, 12, K=(2, 4), length=(1, 3), seed=8)
+    sc = jet.JetScorer(64, 500, wl.N, wl.n_tok)
+    gpu = run_gpu(jet, wl, scorer=sc)
+    compare(wl, gpu, oracle.score_workload(wl))
+
+
+def test_repeat_calls_are_bitwise_deterministic(jet):
+    wl = wk.custom(128, 2500, 30, K=(2, 8), length=(1, 5), seed=21)
+    sc = jet.JetScorer(wl.d, wl.V, wl.N, wl.n_tok)
+    x = to_dev(wl)
+    a = run_gpu(jet, wl, sc, x)
+    b = run_gpu(jet, wl, sc, x)
+    for k in OUT_KEYS:
+        assert np.array_equal(a[k].view(np.uint32), b[k].view(np.uint32)), k
+
+
+def test_host_entry_matches_device_entry(jet):
+    wl = wk.custom(128, 1200, 20, K=(2, 6), length=(1, 4), seed=17)
+    sc = jet.JetScorer(wl.d, wl.V, wl.N, wl.n_tok)
+    x = to_dev(wl)
+    dev = run_gpu(jet, wl, sc, x)
+    cpu = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    host = sc.score_sets_host(cpu(wl.H.view(np.int16)).view(torch.bfloat16), x["W"], cpu(wl.tok_row),
+                              cpu(wl.tok_ids), cpu(wl.cand_offsets), cpu(wl.set_offsets), cpu(wl.kind), wl.T)
+    for k in OUT_KEYS:
+        assert np.array_equal(host[k].numpy().view(np.uint32), dev[k].view(np.uint32)), k
+
+
+def test_outputs_leave_guard_bands_untouched(jet):
+    wl = wk.custom(64, 900, 15, K=(2, 6), length=(1, 4), seed=4)
+    sc = jet.JetScorer(wl.d, wl.V, wl.N, wl.n_tok)
+    x = to_dev(wl)
+    G = 64
+    sizes = dict(logp=wl.n_tok, lse=wl.N, s=wl.n_cand, q=wl.n_cand, q_equiv=wl.n_cand, decision=wl.n_sets,
+                 expected=wl.n_sets, confidence=wl.n_sets, mass=wl.n_sets)
+    bufs, out = {}, {}
+    for k, n in sizes.items():
+        dt = torch.int32 if k == "decision" else torch.float32
+        b = torch.full((n + 2 * G,), -7777, dtype=dt, device="cuda")
+        bufs[k] = b
+        out[k] = b[G:G + n]
+    sc.score_sets(x["H"], x["W"], x["tok_row"], x["tok_ids"], x["cand_offsets"], x["set_offsets"], x["kind"],
+                  wl.T, out=out)
+    torch.cuda.synchronize()
+    for k, b in bufs.items():
+        h = b.cpu().numpy()
+        assert np.all(h[:G] == -7777) and np.all(h[-G:] == -7777), f"{k}: guard band overwritten"
+        assert not np.any(h[G:-G] == -7777), f"{k}: output element not written"
+
+
+# ---------------------------------------------------------------------------
+# the five named workloads at full size (launch configuration of the bench)
+# ---------------------------------------------------------------------------
+def _full_size(jet, wl, sample_sets, threads=0):
+    gpu = run_gpu(jet, wl)
+    sub, set_ids, cands, toks, rows = subset(wl, sample_sets)
+    orc = oracle.score_workload(sub, threads=threads)
+    stats = compare(wl, gpu, orc, set_ids, cands, toks, rows)
+    check_duplicates(wl, gpu)
+    # properties at full size
+    for k in range(wl.n_sets):
+        c0, c1 = wl.set_offsets[k], wl.set_offsets[k + 1]
+        assert abs(gpu["q"][c0:c1].astype(np.float64).sum() - 1.0) < 1e-5
+    assert np.all(np.isfinite(gpu["logp"])) and np.all(gpu["logp"] <= 1e-6)
+    s_from_logp = np.add.reduceat(gpu["logp"].astype(np.float64), wl.cand_offsets[:-1])
+    np.testing.assert_allclose(gpu["s"], s_from_logp, rtol=1e-5, atol=1e-4)
+    return gpu, stats
+
+
+def test_full_size_tiny(jet):
+    wl = wk.tiny()
+    _full_size(jet, wl, range(wl.n_sets))
+
+
+def test_full_size_binary(jet):
+    wl = wk.binary_batch()
+    _full_size(jet, wl, [0, 1, 2, 77, 128, 200, 254, 255])
+    rest = wk.binary_restricted(base=wl)
+    _full_size(jet, rest, range(0, 256, 3))
+
+
+def test_full_size_binary_random_pairs_restricted(jet):
+    wl = wk.binary_restricted(random_pairs=True)
+    _full_size(jet, wl, range(0, 256, 5))
+
+
+def test_full_size_multitoken(jet):
+    wl = wk.multi_token_choice()
+    _full_size(jet, wl, [0, 63])
+
+
+def test_full_size_wideschema(jet):
+    wl = wk.wide_schema()
+    sizes = np.diff(wl.set_offsets)
+    pick = [int(np.argmin(sizes)), 1, 2, int(np.nonzero(wl.kind == wk.KIND_ORDINAL)[0][0])]
+    _full_size(jet, wl, sorted(set(pick)))
+
+
+def test_full_size_large(jet):
+    wl = wk.large_choice()
+    gpu = run_gpu(jet, wl)
+    # sampled tokens: every 700th token's log-probability and its row's lse
+    idx = np.arange(0, wl.n_tok, 700)
+    want = np.zeros(wl.n_tok, np.uint8)
+    want[idx] = 1
+    lp, lse = oracle.score_tokens(wl.H, wl.W, wl.tok_row, wl.tok_ids, want=want)
+    assert np.abs(gpu["logp"][idx] - lp[idx]).max() <= 2e-3
+    rows = wl.tok_row[idx]
+    assert np.abs(gpu["lse"][rows] - lse[rows]).max() <= 2e-3
+    assert check_duplicates(wl, gpu) >= 16 * 3 - 16   # copies per request (a copy may repeat a copy)
+    for k in range(wl.n_sets):
+        c0, c1 = wl.set_offsets[k], wl.set_offsets[k + 1]
+        assert abs(gpu["q"][c0:c1].astype(np.float64).sum() - 1.0) < 1e-5
