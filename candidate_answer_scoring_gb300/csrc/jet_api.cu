@@ -12,6 +12,36 @@
 
 using namespace jet;
 
+namespace jet {
+
+// Choose the number of vocabulary splits S per row tile: every unit is one row
+// tile over n_vt/S vocabulary tiles, units run G at a time, so the busiest CTA
+// processes ceil(n_mt*S/G) * ceil(n_vt/S) tiles; take the smallest such count
+// (ties: fewer splits).  Bands of Gm row tiles keep Gm H tiles (128*d*2 bytes
+// each) within ~48 MB of L2 while the band's units stream W.
+Plan make_plan(int N, int V, int d, int G, int units_cap) {
+  Plan p;
+  p.n_mt = (N + BM - 1) / BM;
+  p.n_vt = (V + BN - 1) / BN;
+  const int S_max = std::max(1, std::min(p.n_vt, units_cap / std::max(1, p.n_mt)));
+  long long best = -1;
+  for (int S = 1; S <= S_max; ++S) {
+    const long long waves = ((long long)p.n_mt * S + G - 1) / G;
+    const long long t = waves * ((p.n_vt + S - 1) / S);
+    if (best < 0 || t < best) { best = t; p.S = S; }
+  }
+  const long long a_tile = (long long)BM * d * 2;
+  const int gm_max = (int)std::max(1LL, (48LL << 20) / a_tile);
+  p.Gm = std::max(1, std::min(p.n_mt, gm_max));
+  p.n_full_bands = p.n_mt / p.Gm;
+  p.r_last = p.n_mt - p.n_full_bands * p.Gm;
+  p.units = p.n_mt * p.S;
+  p.grid = std::min(p.units, G);
+  return p;
+}
+
+}  // namespace jet
+
 namespace {
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -73,32 +103,6 @@ struct DeviceGuard {
     if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
   }
 };
-
-// Choose the number of vocabulary splits S per row tile: every unit is one row
-// tile over n_vt/S vocabulary tiles, units run G at a time, so the busiest CTA
-// processes ceil(n_mt*S/G) * ceil(n_vt/S) tiles; take the smallest such count
-// (ties: fewer splits).  Bands of Gm row tiles keep Gm H tiles (128*d*2 bytes
-// each) within ~48 MB of L2 while the band's units stream W.
-Plan make_plan(int N, int V, int d, int G, int units_cap) {
-  Plan p;
-  p.n_mt = (N + BM - 1) / BM;
-  p.n_vt = (V + BN - 1) / BN;
-  const int S_max = std::max(1, std::min(p.n_vt, units_cap / std::max(1, p.n_mt)));
-  long long best = -1;
-  for (int S = 1; S <= S_max; ++S) {
-    const long long waves = ((long long)p.n_mt * S + G - 1) / G;
-    const long long t = waves * ((p.n_vt + S - 1) / S);
-    if (best < 0 || t < best) { best = t; p.S = S; }
-  }
-  const long long a_tile = (long long)BM * d * 2;
-  const int gm_max = (int)std::max(1LL, (48LL << 20) / a_tile);
-  p.Gm = std::max(1, std::min(p.n_mt, gm_max));
-  p.n_full_bands = p.n_mt / p.Gm;
-  p.r_last = p.n_mt - p.n_full_bands * p.Gm;
-  p.units = p.n_mt * p.S;
-  p.grid = std::min(p.units, G);
-  return p;
-}
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? JET_OK : JET_ERR_CUDA; }
 

@@ -48,6 +48,9 @@ struct HeadArgs {
   int* err;
 };
 
+// Host: schedule for N rows with at most units_cap units on G SMs.
+Plan make_plan(int N, int V, int d, int G, int units_cap);
+
 // Decode unit u of the plan into (row tile, first vocab tile, end vocab tile).
 __host__ __device__ __forceinline__ void plan_unit(const Plan& p, int u, int& m, int& vt0, int& vt1) {
   const int main_units = p.n_full_bands * p.Gm * p.S;

@@ -199,6 +199,31 @@ int jet_plan_info(jet_ctx *ctx, int n_rows, int *info8);
 int jet_profile_enable(jet_ctx *ctx, int enable);
 int jet_profile_read(jet_ctx *ctx, double *out, int n_out);
 
+/*
+ * jet_score_tokens_noalloc: the computation of jet_score_tokens (one scored
+ * token per row, logp[i] = z[i, tok_ids[i]] - lse[i]) for callers that cannot
+ * allocate device memory -- code running inside a process whose device memory
+ * belongs to another framework's pool allocator (an inference server or a
+ * plugin that reserves memory up front), where cudaMalloc may fail or stall
+ * all streams with its implicit synchronisation mid-request.  It needs no
+ * context and calls no allocating routine.  The pages describing the method
+ * have no counterpart to this entry point.
+ *
+ * Arguments as jet_score_tokens, plus the embedding shape d, V (same limits as
+ * jet_create); works on the CURRENT CUDA device.  Scratch lives in one static
+ * device array of about 2.2 MB that every GPU loading the library keeps until
+ * the process exits; it bounds a call to n_pos <= JET_NOALLOC_MAX_POS
+ * (larger batches return JET_ERR_WORKSPACE).  All calls share that array:
+ * calls whose GPU work overlaps (other streams or host threads) race on it.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) and caches it; make that first call before any
+ * stream capture.  Synchronous; returns JET_OK or a status as above.
+ */
+#define JET_NOALLOC_MAX_POS 4096
+#define JET_NOALLOC_MAX_UNITS 1024
+int jet_score_tokens_noalloc(const void *H_bf16, const void *W_bf16, int d, int V, const int32_t *tok_ids,
+                             int n_pos, float *logp, float *lse, void *cuda_stream);
+
 #ifdef __cplusplus
 }
 #endif
