@@ -40,6 +40,22 @@ Plan make_plan(int N, int V, int d, int G, int units_cap) {
   return p;
 }
 
+int head_prefetch_kblocks(const Plan& p) {
+  static int env = -2;
+  if (env == -2) {
+    const char* v = std::getenv("JETSCORE_W_PREFETCH");
+    env = v ? std::atoi(v) : -1;
+  }
+  (void)p;
+  return env > 0 ? env : 0;
+}
+
+bool pdl_enabled() {
+  static int on = -1;
+  if (on < 0) on = std::getenv("JETSCORE_NO_PDL") ? 0 : 1;
+  return on == 1;
+}
+
 }  // namespace jet
 
 namespace {
@@ -175,6 +191,7 @@ int run_full_head(jet_ctx* c, const void* H, const void* W, int n_rows, float* l
   ha.zg = c->zg;
   ha.part = c->part;
   ha.err = c->err;
+  ha.pf_kblocks = head_prefetch_kblocks(ha.plan);
   cudaError_t e;
   {
     ProfScope ps(c, K_HEAD, st);
@@ -428,6 +445,18 @@ int jet_profile_read(jet_ctx* c, double* out, int n_out) {
   if (n_out > 10) out[10] = c->untimed;
   c->untimed = 0;
   return rc;
+}
+
+int jet_selftest_wait_timeout(jet_ctx* c, int limit_us, void* stream) {
+  if (!c || limit_us < 1 || limit_us > 2000000) return JET_ERR_ARG;
+  DeviceGuard g(c->device);
+  if (!g.ok) return JET_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (launch_wait_selftest(c->err, 1000ull * (unsigned long long)limit_us, st) != cudaSuccess) return JET_ERR_CUDA;
+  if (cudaMemcpyAsync(c->h_err, c->err, ERR_WORDS * sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return JET_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return JET_ERR_CUDA;
+  return (c->h_err[0] == JET_ERR_TIMEOUT && c->h_err[2] == 99) ? JET_ERR_TIMEOUT : JET_ERR_CUDA;
 }
 
 int jet_plan_info(jet_ctx* c, int n_rows, int* info) {

@@ -30,6 +30,35 @@ __device__ __forceinline__ void set_error(int* err, int code, int detail) {
   if (atomicCAS(err, 0, code) == 0) err[1] = detail;
 }
 
+// Programmatic dependent launch: kernels of one call are launched so that the
+// next may be scheduled while the previous is still running.  A kernel calls
+// pdl_wait() before it reads anything the previous kernel writes (including
+// the error word); pdl_wait() returns at once when there is no dependency.
+// pdl_trigger() lets the next kernel start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Programmatic dependent launch is on unless the environment variable
+// JETSCORE_NO_PDL is set (a diagnostic: launches then serialise normally).
+bool pdl_enabled();
+
+// Launch `kernel` on `st` as a programmatic dependent of the preceding kernel.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                             Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // Vocabulary-split schedule of the head: unit u = (row tile m, split s) covers
 // vocabulary tiles [s*n_vt/S, (s+1)*n_vt/S).  Units are ordered band by band
 // (Gm row tiles per band), split-major inside a band, so CTAs running together
@@ -46,10 +75,17 @@ struct HeadArgs {
   float* zg;            // [n_tok] gathered logit of each scored token
   float2* part;         // [units*2*BM] per (unit, column half, row): (max, sum exp(z - max))
   int* err;
+  int pf_kblocks;       // L2 prefetch distance for W, in k-blocks of the CTA's stream (0: off)
 };
 
 // Host: schedule for N rows with at most units_cap units on G SMs.
 Plan make_plan(int N, int V, int d, int G, int units_cap);
+
+// Host: L2 prefetch distance (k-blocks) for the head's W stream.  Off by
+// default: measured on GB300 it slowed the W-streaming head (two CTAs share
+// each W tile and both prefetch).  The environment variable
+// JETSCORE_W_PREFETCH sets a distance for experiments.
+int head_prefetch_kblocks(const Plan& p);
 
 // Decode unit u of the plan into (row tile, first vocab tile, end vocab tile).
 __host__ __device__ __forceinline__ void plan_unit(const Plan& p, int u, int& m, int& vt0, int& vt1) {
@@ -124,5 +160,9 @@ struct SetArgs {
   const int* err;
 };
 cudaError_t launch_sets(const SetArgs& a, cudaStream_t st);
+
+// One CTA waits on an mbarrier that nothing completes, with a limit of
+// limit_ns; the bounded wait records JET_ERR_TIMEOUT (where = 99) in err.
+cudaError_t launch_wait_selftest(int* err, unsigned long long limit_ns, cudaStream_t st);
 
 }  // namespace jet

@@ -145,6 +145,7 @@ extern "C" int jet_score_tokens_noalloc(const void* H, const void* W, int d, int
   ha.zg = zg;
   ha.part = part;
   ha.err = err;
+  ha.pf_kblocks = head_prefetch_kblocks(ha.plan);
   if (launch_head(tmH, tmW, ha, st) != cudaSuccess) {
     cudaStreamSynchronize(st);
     return JET_ERR_CUDA;

@@ -24,68 +24,12 @@
 #include <climits>
 
 #include "jet_internal.cuh"
+#include "jet_wait.cuh"
 
 namespace jet {
 namespace {
 
 constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;   // 2 s per wait
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ unsigned long long globaltimer() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-// ---- mbarrier ----------------------------------------------------------------
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Bounded wait for the phase of `bar` with the given parity.  Returns false if
-// another role asked to abort or if the wait exceeded WAIT_LIMIT_NS (then it
-// raises the abort flag and, when err is given, records where in err[2]).
-__device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err,
-                                       int where) {
-  const uint32_t a = smem_u32(bar);
-  if (mbar_try_wait(a, parity)) return true;
-  const unsigned long long t0 = globaltimer();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(a, parity)) return true;
-    if ((it & 63u) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer() - t0 > WAIT_LIMIT_NS) {
-        *abort_flag = 1;
-        if (err != nullptr && atomicCAS(err, 0, JET_ERR_TIMEOUT) == 0) err[2] = where;
-        return false;
-      }
-    }
-  }
-}
 
 // ---- TMA ----------------------------------------------------------------------
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
@@ -94,6 +38,14 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
       : "memory");
+}
+
+// Bring a tile into L2 ahead of its TMA load (no shared-memory destination).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
 }
 
 // ---- tcgen05 ------------------------------------------------------------------
@@ -190,7 +142,7 @@ __global__ void __launch_bounds__(HEAD_THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (*(volatile const int*)a.err != 0) return;   // pre-pass rejected the batch (uniform)
+  pdl_trigger();   // the merge kernel may be scheduled; it waits for this grid to finish
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
@@ -231,10 +183,15 @@ __global__ void __launch_bounds__(HEAD_THREADS, 1)
         for (int vt = vt0; ok && vt < vt1; ++vt) {
           if (*abort_flag) { ok = false; break; }
           for (int kb = 0; kb < kblocks; ++kb) {
-            if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.err, 1)) { ok = false; break; }
+            if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.err, 1, WAIT_LIMIT_NS)) { ok = false; break; }
             mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
             tma_load_2d(sA + stage * A_STAGE_BYTES, &tmH, kb * BK, m * BM, &full[stage]);
             tma_load_2d(sB + stage * B_STAGE_BYTES, &tmW, kb * BK, vt * BN, &full[stage]);
+            if (a.pf_kblocks > 0) {   // keep more W bytes in flight to DRAM than the ring holds
+              const int ip = (vt - vt0) * kblocks + kb + a.pf_kblocks;
+              const int vtp = vt0 + ip / kblocks;
+              if (vtp < vt1) tma_prefetch_l2_2d(&tmW, (ip % kblocks) * BK, vtp * BN);
+            }
             issued_mask |= 1u << stage;
             issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
             if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -245,14 +202,14 @@ __global__ void __launch_bounds__(HEAD_THREADS, 1)
         // tail: wait until the MMA has released every stage, so that no
         // barrier arrival is still pending when the CTA exits
         for (int i = 0; i < STAGES; ++i) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.err, 5)) break;
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.err, 5, WAIT_LIMIT_NS)) break;
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
       } else {
         // abort: let copies already in flight land before the CTA exits
         volatile int never = 0;
         for (int s = 0; s < STAGES; ++s)
-          if (issued_mask & (1u << s)) mbar_wait(&full[s], (issued_parity >> s) & 1u, &never, nullptr, 0);
+          if (issued_mask & (1u << s)) mbar_wait(&full[s], (issued_parity >> s) & 1u, &never, nullptr, 0, WAIT_LIMIT_NS);
       }
     }
   } else if (warp == 1) {
@@ -265,11 +222,11 @@ __global__ void __launch_bounds__(HEAD_THREADS, 1)
         int m, vt0, vt1;
         plan_unit(P, u, m, vt0, vt1);
         for (int vt = vt0; ok && vt < vt1; ++vt) {
-          if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, a.err, 2)) { ok = false; break; }
+          if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, a.err, 2, WAIT_LIMIT_NS)) { ok = false; break; }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
           for (int kb = 0; kb < kblocks; ++kb) {
-            if (!mbar_wait(&full[stage], phase, abort_flag, a.err, 3)) { ok = false; break; }
+            if (!mbar_wait(&full[stage], phase, abort_flag, a.err, 3, WAIT_LIMIT_NS)) { ok = false; break; }
             tc_fence_after();
             const uint32_t a0 = smem_u32(sA + stage * A_STAGE_BYTES);
             const uint32_t b0 = smem_u32(sB + stage * B_STAGE_BYTES);
@@ -289,7 +246,7 @@ __global__ void __launch_bounds__(HEAD_THREADS, 1)
       if (!ok && any) {   // wait until every MMA issued so far has completed
         volatile int never = 0;
         tc_commit(drain);
-        mbar_wait(drain, 0, &never, nullptr, 0);
+        mbar_wait(drain, 0, &never, nullptr, 0, WAIT_LIMIT_NS);
       }
     }
   } else {
@@ -299,7 +256,9 @@ __global__ void __launch_bounds__(HEAD_THREADS, 1)
     const int row_in_tile = quarter * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
-    bool ok = true;
+    pdl_wait();   // row lists and the error word come from the pre-pass
+    bool ok = *(volatile const int*)a.err == 0;
+    if (!ok) *abort_flag = 1;   // pre-pass rejected the batch: every role stops
     for (int u = blockIdx.x; ok && u < P.units; u += gridDim.x) {
       int m, vt0, vt1;
       plan_unit(P, u, m, vt0, vt1);
@@ -315,7 +274,7 @@ __global__ void __launch_bounds__(HEAD_THREADS, 1)
       }
       float m_run = -INFINITY, s_run = 0.f;
       for (int vt = vt0; vt < vt1; ++vt) {
-        if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, a.err, 4)) { ok = false; break; }
+        if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, a.err, 4, WAIT_LIMIT_NS)) { ok = false; break; }
         tc_fence_after();
         const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN + half * 128);
         const int col0 = vt * BN + half * 128;
@@ -387,8 +346,8 @@ cudaError_t launch_head(const CUtensorMap& tmH, const CUtensorMap& tmW, const He
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  head_lse_gather_kernel<<<a.plan.grid, HEAD_THREADS, HEAD_SMEM_BYTES, st>>>(tmH, tmW, a);
-  return cudaGetLastError();
+  return launch_dependent(head_lse_gather_kernel, dim3(a.plan.grid), dim3(HEAD_THREADS), HEAD_SMEM_BYTES, st, tmH,
+                          tmW, a);
 }
 
 }  // namespace jet

@@ -1,6 +1,9 @@
 // Device pre-pass: validates every index the rest of the path will use and
 // builds, per hidden row, the list of scored tokens it predicts (sorted by
 // token id), which the head's epilogue walks while it sweeps vocabulary tiles.
+// Three layouts: one token per row (jet_score_tokens), tokens already grouped
+// by row (tok_row non-decreasing: row pointers from run boundaries), and the
+// general case (count, scan, scatter).
 //
 // One CTA of 1024 threads: the work is O(n_tok + n_rows + n_cand) integer
 // operations, a few microseconds, and a single CTA needs no inter-CTA
@@ -12,37 +15,48 @@ namespace jet {
 namespace {
 
 constexpr int PREP_THREADS = 1024;
+constexpr int PREP_SMEM_ROWS = 6144;   // per-row counters in shared memory up to this many rows
 
 __device__ __forceinline__ int row_of(const PrepArgs& a, int j) {
   return a.tok_row ? a.tok_row[j] : j;
 }
 
+// Dynamic shared memory: [n_union] union ids (restricted mode), then
+// [n_rows + 1] per-row counters when SMEM_COUNTS.  Kept small so that the
+// head kernel's CTA can share an SM with this one while it starts.
+template <bool SMEM_COUNTS>
 __global__ void __launch_bounds__(PREP_THREADS) prep_kernel(PrepArgs a) {
-  __shared__ int s_union[JET_MAX_UNION];
-  __shared__ int s_scan[PREP_THREADS];
-  const int tid = threadIdx.x, nth = blockDim.x;
+  extern __shared__ int s_dyn[];
+  __shared__ int s_warp[PREP_THREADS / 32];
+  __shared__ int s_unsorted;
+  int* s_union = s_dyn;
+  int* s_cnt = s_dyn + (a.mode == JET_MODE_RESTRICTED ? a.n_union : 0);
+  const int tid = threadIdx.x, nth = blockDim.x, lane = tid & 31, warp = tid >> 5;
+  pdl_trigger();   // the head may start its loads and MMAs; it waits before reading our outputs
   int* err = a.err;
+  int* cnt = SMEM_COUNTS ? s_cnt : a.row_cur;
+  const bool identity = a.tok_row == nullptr;    // token i is predicted by row i
 
   if (tid == 0) {
     for (int i = 0; i < ERR_WORDS; ++i) err[i] = 0;
+    s_unsorted = 0;
   }
-  for (int r = tid; r <= a.n_rows; r += nth) a.row_cur[r] = 0;
+  if (a.mode == JET_MODE_RESTRICTED)
+    for (int u = tid; u < a.n_union; u += nth) s_union[u] = a.union_ids[u];
   __syncthreads();
 
-  // scored tokens: id in [0, V), row in [0, n_rows); count tokens per row
+  // scored tokens: id in [0, V), row in [0, n_rows); is tok_row non-decreasing?
   for (int j = tid; j < a.n_tok; j += nth) {
     const int t = a.tok_ids[j], r = row_of(a, j);
     if (t < 0 || t >= a.V || r < 0 || r >= a.n_rows) set_error(err, JET_ERR_TOKEN_RANGE, j);
-    else atomicAdd(&a.row_cur[r], 1);
+    if (!identity && j > 0 && a.tok_row[j - 1] > r) s_unsorted = 1;
   }
 
   // candidate and set offsets (CSR), kind constraints
   if (a.cand_offsets) {
     if (tid == 0) {
-      if (a.cand_offsets[0] != 0 || a.cand_offsets[a.n_cand] != a.n_tok)
-        set_error(err, JET_ERR_OFFSETS, 0);
-      if (a.set_offsets[0] != 0 || a.set_offsets[a.n_sets] != a.n_cand)
-        set_error(err, JET_ERR_OFFSETS, 0);
+      if (a.cand_offsets[0] != 0 || a.cand_offsets[a.n_cand] != a.n_tok) set_error(err, JET_ERR_OFFSETS, 0);
+      if (a.set_offsets[0] != 0 || a.set_offsets[a.n_sets] != a.n_cand) set_error(err, JET_ERR_OFFSETS, 0);
     }
     for (int c = tid; c < a.n_cand; c += nth) {
       const int len = a.cand_offsets[c + 1] - a.cand_offsets[c];
@@ -62,11 +76,10 @@ __global__ void __launch_bounds__(PREP_THREADS) prep_kernel(PrepArgs a) {
   // restricted mode: union ids in range and distinct; every token in the union
   if (a.mode == JET_MODE_RESTRICTED) {
     for (int u = tid; u < a.n_union; u += nth) {
-      const int t = a.union_ids[u];
-      s_union[u] = t;
+      const int t = s_union[u];
       if (t < 0 || t >= a.V) set_error(err, JET_ERR_TOKEN_RANGE, u);
     }
-    __syncthreads();
+    __syncthreads();                                 // range errors take precedence
     for (int u = tid; u < a.n_union; u += nth)
       for (int w = 0; w < u; ++w)
         if (s_union[w] == s_union[u]) set_error(err, JET_ERR_NOT_IN_UNION, u);
@@ -82,33 +95,83 @@ __global__ void __launch_bounds__(PREP_THREADS) prep_kernel(PrepArgs a) {
   __syncthreads();
   if (*(volatile int*)err != 0) return;
 
-  // exclusive scan of the per-row counts -> row_ptr; row_cur becomes the cursor
+  if (identity) {                                    // one token per row, in row order
+    for (int i = tid; i < a.n_tok; i += nth) {
+      a.row_ptr[i] = i;
+      a.row_list[i] = make_int2(a.tok_ids[i], i);
+    }
+    if (tid == 0) a.row_ptr[a.n_rows] = a.n_tok;
+    return;
+  }
+
+  if (!s_unsorted) {
+    // tokens already grouped by row: row_ptr from the run boundaries of tok_row
+    for (int j = tid; j < a.n_tok; j += nth) {
+      const int r = a.tok_row[j];
+      const int rp = (j == 0) ? -1 : a.tok_row[j - 1];
+      for (int rr = rp + 1; rr <= r; ++rr) a.row_ptr[rr] = j;       // rows rp+1 .. r start at j
+      if (j == a.n_tok - 1)
+        for (int rr = r + 1; rr <= a.n_rows; ++rr) a.row_ptr[rr] = a.n_tok;
+      a.row_list[j] = make_int2(a.tok_ids[j], j);
+    }
+    __syncthreads();
+    for (int r = tid; r < a.n_rows; r += nth) {      // order each row's tokens by id
+      const int b = a.row_ptr[r], e = a.row_ptr[r + 1];
+      for (int i = b + 1; i < e; ++i) {
+        const int2 x = a.row_list[i];
+        int k = i - 1;
+        while (k >= b && (a.row_list[k].x > x.x || (a.row_list[k].x == x.x && a.row_list[k].y > x.y))) {
+          a.row_list[k + 1] = a.row_list[k];
+          --k;
+        }
+        a.row_list[k + 1] = x;
+      }
+    }
+    return;
+  }
+
+  // general layout: count tokens per row
+  for (int r = tid; r <= a.n_rows; r += nth) cnt[r] = 0;
+  __syncthreads();
+  for (int j = tid; j < a.n_tok; j += nth) atomicAdd(&cnt[a.tok_row[j]], 1);
+  __syncthreads();
+
+  // exclusive scan of the per-row counts -> row_ptr; the counters become cursors
   const int chunk = (a.n_rows + nth - 1) / nth;
   const int r0 = min(a.n_rows, tid * chunk), r1 = min(a.n_rows, r0 + chunk);
   int local = 0;
-  for (int r = r0; r < r1; ++r) local += a.row_cur[r];
-  s_scan[tid] = local;
-  __syncthreads();
-  for (int off = 1; off < nth; off <<= 1) {        // Hillis-Steele inclusive scan
-    const int v = (tid >= off) ? s_scan[tid - off] : 0;
-    __syncthreads();
-    s_scan[tid] += v;
-    __syncthreads();
+  for (int r = r0; r < r1; ++r) local += cnt[r];
+  int incl = local;                                  // inclusive scan within the warp
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
   }
-  int run = s_scan[tid] - local;
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = (lane < nth / 32) ? s_warp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += v;
+    }
+    s_warp[lane] = w;                                // inclusive warp totals
+  }
+  __syncthreads();
+  int run = incl - local + (warp > 0 ? s_warp[warp - 1] : 0);
   for (int r = r0; r < r1; ++r) {
-    const int c = a.row_cur[r];
+    const int c = cnt[r];
     a.row_ptr[r] = run;
-    a.row_cur[r] = run;
+    cnt[r] = run;
     run += c;
   }
-  if (tid == nth - 1) a.row_ptr[a.n_rows] = s_scan[nth - 1];
+  if (tid == nth - 1) a.row_ptr[a.n_rows] = s_warp[nth / 32 - 1];
   __syncthreads();
 
   // scatter (token id, token index) into each row's slot range
   for (int j = tid; j < a.n_tok; j += nth) {
-    const int r = row_of(a, j);
-    const int pos = atomicAdd(&a.row_cur[r], 1);
+    const int pos = atomicAdd(&cnt[row_of(a, j)], 1);
     a.row_list[pos] = make_int2(a.tok_ids[j], j);
   }
   __syncthreads();
@@ -131,7 +194,11 @@ __global__ void __launch_bounds__(PREP_THREADS) prep_kernel(PrepArgs a) {
 }  // namespace
 
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t st) {
-  prep_kernel<<<1, PREP_THREADS, 0, st>>>(a);
+  const size_t union_bytes = (a.mode == JET_MODE_RESTRICTED ? (size_t)a.n_union : 0) * sizeof(int);
+  if (a.tok_row != nullptr && a.n_rows + 1 <= PREP_SMEM_ROWS)
+    prep_kernel<true><<<1, PREP_THREADS, union_bytes + (a.n_rows + 1) * sizeof(int), st>>>(a);
+  else
+    prep_kernel<false><<<1, PREP_THREADS, union_bytes, st>>>(a);
   return cudaGetLastError();
 }
 

@@ -9,33 +9,53 @@ namespace jet {
 namespace {
 
 // ---------------------------------------------------------------------------
-// lse[r] = M + log sum_i s_i exp(m_i - M) over the 2*S partials of row r, in a
-// fixed order (so identical rows give bit-identical results), then
-// logp[j] = z[r, tok_j] - lse[r] for the row's tokens
-// ("JET: Justification Evaluation in Transformer", Eq. 2).
-// One thread per row.
+// lse[r] = M + log sum_i s_i exp(m_i - M) over the 2*S partials of row r
+// ("JET: Justification Evaluation in Transformer", Eq. 2), then
+// logp[j] = z[r, tok_j] - lse[r] for the row's tokens.  One warp per row:
+// lane l folds partials l, l+32, ... into a running (max, sum), and the lanes
+// combine in a fixed butterfly, so identical rows give bit-identical results.
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ void lse_fold(float& m, float& s, float m2, float s2) {
+  const float mn = fmaxf(m, m2);
+  if (mn == -INFINITY) return;                       // both empty
+  s = s * expf(m - mn) + s2 * expf(m2 - mn);
+  m = mn;
+}
+
 __global__ void __launch_bounds__(256) merge_kernel(const MergeArgs a) {
-  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  pdl_trigger();
+  pdl_wait();
   if (*(volatile const int*)a.err != 0 || r >= a.N) return;
   const Plan& P = a.plan;
-  const int m = r / BM, lr = r - m * BM;
-  float M = -INFINITY;
-  for (int sp = 0; sp < P.S; ++sp) {
-    const size_t u = (size_t)plan_unit_of(P, m, sp);
-    for (int h = 0; h < 2; ++h) M = fmaxf(M, a.part[(u * 2 + h) * BM + lr].x);
-  }
-  float sum = 0.f;
-  for (int sp = 0; sp < P.S; ++sp) {
-    const size_t u = (size_t)plan_unit_of(P, m, sp);
-    for (int h = 0; h < 2; ++h) {
-      const float2 p = a.part[(u * 2 + h) * BM + lr];
-      if (p.x != -INFINITY) sum += p.y * expf(p.x - M);
+  const int m_tile = r / BM, lr = r - m_tile * BM;
+  float m = -INFINITY, s = 0.f;
+  const int n_slots = 2 * P.S;
+  int slot = lane;
+  for (; slot + 96 < n_slots; slot += 128) {        // four independent loads in flight
+    float2 p[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int sl = slot + 32 * i;
+      p[i] = a.part[((size_t)plan_unit_of(P, m_tile, sl >> 1) * 2 + (sl & 1)) * BM + lr];
     }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) lse_fold(m, s, p[i].x, p[i].y);
   }
-  const float lse = M + logf(sum);
-  if (a.lse) a.lse[r] = lse;
-  for (int e = a.row_ptr[r]; e < a.row_ptr[r + 1]; ++e) {
+  for (; slot < n_slots; slot += 32) {
+    const float2 p = a.part[((size_t)plan_unit_of(P, m_tile, slot >> 1) * 2 + (slot & 1)) * BM + lr];
+    lse_fold(m, s, p.x, p.y);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    lse_fold(m, s, m2, s2);
+  }
+  const float lse = m + logf(s);
+  if (lane == 0 && a.lse) a.lse[r] = lse;
+  for (int e = a.row_ptr[r] + lane; e < a.row_ptr[r + 1]; e += 32) {
     const int j = a.row_list[e].y;
     a.logp[j] = a.zg[j] - lse;
   }
@@ -58,31 +78,137 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 __device__ __forceinline__ bool same_sequence(const int32_t* tok, const int32_t* co, int a, int b) {
-  const int la = co[a + 1] - co[a], lb = co[b + 1] - co[b];
-  if (la != lb) return false;
-  for (int t = 0; t < la; ++t)
-    if (tok[co[a] + t] != tok[co[b] + t]) return false;
-  return true;
+  const int a0 = co[a], b0 = co[b], la = co[a + 1] - a0;
+  if (la != co[b + 1] - b0) return false;
+  bool same = true;
+  for (int t = 0; t < la; ++t) same &= (tok[a0 + t] == tok[b0 + t]);   // no early exit: loads overlap
+  return same;
+}
+
+// s(c) and the FNV-1a hash of c's token sequence (length folded in first).
+__device__ __forceinline__ float chain_sum(const SetArgs& a, int c, unsigned long long& h) {
+  const int t0 = a.cand_offsets[c], t1 = a.cand_offsets[c + 1];
+  h = 1469598103934665603ull ^ (unsigned long long)(t1 - t0);
+  float acc = 0.f;
+  int t = t0;
+  for (; t + 4 <= t1; t += 4) {            // four independent loads in flight
+    const float l0 = a.logp[t], l1 = a.logp[t + 1], l2 = a.logp[t + 2], l3 = a.logp[t + 3];
+    const int k0 = a.tok_ids[t], k1 = a.tok_ids[t + 1], k2 = a.tok_ids[t + 2], k3 = a.tok_ids[t + 3];
+    acc += l0; acc += l1; acc += l2; acc += l3;   // token order
+    h = (h ^ (unsigned long long)(uint32_t)k0) * 1099511628211ull;
+    h = (h ^ (unsigned long long)(uint32_t)k1) * 1099511628211ull;
+    h = (h ^ (unsigned long long)(uint32_t)k2) * 1099511628211ull;
+    h = (h ^ (unsigned long long)(uint32_t)k3) * 1099511628211ull;
+  }
+  for (; t < t1; ++t) {
+    acc += a.logp[t];
+    h = (h ^ (unsigned long long)(uint32_t)a.tok_ids[t]) * 1099511628211ull;
+  }
+  return acc;
+}
+
+// Set rules for K <= 32*CPL candidates held in registers: candidate i of the
+// set lives in lane i % 32, slot i / 32.
+template <int CPL>
+__device__ __forceinline__ void set_rules_regs(const SetArgs& a, int set, int lane, int c0, int K, float invT) {
+  float sc[CPL], q[CPL];
+  unsigned long long h[CPL];
+  float best = -INFINITY;
+  int best_i = INT_MAX;
+#pragma unroll
+  for (int k = 0; k < CPL; ++k) {
+    const int i = k * 32 + lane;
+    sc[k] = -INFINITY;
+    h[k] = 0;
+    if (i < K) {
+      sc[k] = chain_sum(a, c0 + i, h[k]);
+      a.s[c0 + i] = sc[k];
+      if (sc[k] > best) { best = sc[k]; best_i = i; }      // i grows with k: first maximum kept
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, best_i, o);
+    if (ob > best || (ob == best && oi < best_i)) { best = ob; best_i = oi; }
+  }
+  float z = 0.f;
+#pragma unroll
+  for (int k = 0; k < CPL; ++k) {
+    q[k] = (k * 32 + lane < K) ? expf((sc[k] - best) * invT) : 0.f;
+    z += q[k];
+  }
+  const float Z = warp_sum(z);
+  float ex = 0.f, ent = 0.f;
+#pragma unroll
+  for (int k = 0; k < CPL; ++k) {
+    q[k] /= Z;
+    ex += (float)(k * 32 + lane) * q[k];
+    if (q[k] > 0.f) ent -= q[k] * logf(q[k]);
+  }
+  ex = warp_sum(ex);
+  ent = warp_sum(ent);
+  float qe[CPL], mass_l = 0.f;
+  bool first[CPL];
+#pragma unroll
+  for (int k = 0; k < CPL; ++k) { qe[k] = 0.f; first[k] = true; }
+  for (int j = 0; j < K; ++j) {             // candidate j: lane j % 32, slot j / 32
+    const int src = j & 31, slot = j >> 5;
+    unsigned long long hj = 0;
+    float qj = 0.f;
+#pragma unroll
+    for (int k = 0; k < CPL; ++k) {
+      const unsigned long long hk = __shfl_sync(0xffffffffu, h[k], src);
+      const float qk = __shfl_sync(0xffffffffu, q[k], src);
+      if (k == slot) { hj = hk; qj = qk; }
+    }
+#pragma unroll
+    for (int k = 0; k < CPL; ++k) {
+      const int i = k * 32 + lane;
+      // a candidate is its own class member; others are compared only on a hash match
+      if (i < K && hj == h[k] && (j == i || same_sequence(a.tok_ids, a.cand_offsets, c0 + i, c0 + j))) {
+        qe[k] += qj;
+        if (j < i) first[k] = false;
+      }
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < CPL; ++k) {
+    const int i = k * 32 + lane;
+    if (i < K) {
+      a.q[c0 + i] = q[k];
+      a.q_equiv[c0 + i] = qe[k];
+      if (first[k]) mass_l += expf(sc[k]);
+    }
+  }
+  const float mass = warp_sum(mass_l);
+  if (lane == 0) {
+    a.decision[set] = best_i;
+    a.expected[set] = ex;
+    a.confidence[set] = (K == 1) ? 1.0f : 1.0f - ent / logf((float)K);
+    a.mass[set] = mass;
+  }
 }
 
 __global__ void __launch_bounds__(256) sets_kernel(const SetArgs a) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
+  pdl_wait();
   if (*(volatile const int*)a.err != 0 || warp >= a.n_sets) return;
   const int c0 = a.set_offsets[warp], c1 = a.set_offsets[warp + 1], K = c1 - c0;
   const float invT = 1.0f / a.T;
 
+  if (K <= 32) { set_rules_regs<1>(a, warp, lane, c0, K, invT); return; }
+  if (K <= 64) { set_rules_regs<2>(a, warp, lane, c0, K, invT); return; }
+  if (K <= 128) { set_rules_regs<4>(a, warp, lane, c0, K, invT); return; }
+
+  // larger sets: the same passes through global memory
   // pass 1: chain rule, sequence hash, first argmax
   float best = -INFINITY;
   int best_i = INT_MAX;
   for (int c = c0 + lane; c < c1; c += 32) {
-    const int t0 = a.cand_offsets[c], t1 = a.cand_offsets[c + 1];
-    float acc = 0.f;
-    unsigned long long h = 1469598103934665603ull ^ (unsigned long long)(t1 - t0);
-    for (int t = t0; t < t1; ++t) {
-      acc += a.logp[t];
-      h = (h ^ (unsigned long long)(uint32_t)a.tok_ids[t]) * 1099511628211ull;
-    }
+    unsigned long long h;
+    const float acc = chain_sum(a, c, h);
     a.s[c] = acc;
     a.hash[c] = h;
     if (acc > best || (acc == best && c < best_i)) { best = acc; best_i = c; }
@@ -118,7 +244,7 @@ __global__ void __launch_bounds__(256) sets_kernel(const SetArgs a) {
     float qe = 0.f;
     bool first = true;
     for (int c2 = c0; c2 < c1; ++c2) {
-      if (a.hash[c2] == hc && same_sequence(a.tok_ids, a.cand_offsets, c, c2)) {
+      if (a.hash[c2] == hc && (c2 == c || same_sequence(a.tok_ids, a.cand_offsets, c, c2))) {
         qe += a.q[c2];
         if (c2 < c) first = false;
       }
@@ -140,15 +266,14 @@ __global__ void __launch_bounds__(256) sets_kernel(const SetArgs a) {
 
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t st) {
   if (a.N <= 0) return cudaSuccess;
-  merge_kernel<<<(a.N + 255) / 256, 256, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_dependent(merge_kernel, dim3((a.N + 7) / 8), dim3(256), 0, st, a);   // one warp per row
 }
 
 cudaError_t launch_sets(const SetArgs& a, cudaStream_t st) {
   if (a.n_sets <= 0) return cudaSuccess;
   const int warps_per_block = 8;
-  sets_kernel<<<(a.n_sets + warps_per_block - 1) / warps_per_block, 32 * warps_per_block, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_dependent(sets_kernel, dim3((a.n_sets + warps_per_block - 1) / warps_per_block),
+                          dim3(32 * warps_per_block), 0, st, a);
 }
 
 }  // namespace jet

@@ -9,10 +9,14 @@
 // The set rules then run unchanged; within a set sharing one row, lse_U
 // cancels and q = softmax(z / T) over the set's codes (step 6).
 //
-// Work is tiny (|U| is tens of codes); the kernel is launch-latency bound.  A
-// CTA stages R hidden rows and chunks of the gathered W_U rows in shared
-// memory; one warp per row computes the |U| dot products (lane-strided over d
-// in 16-byte vectors, fixed-order warp reduction) into shared memory.
+// Work is tiny (|U| is tens of codes) and latency-bound, so the kernel
+// spreads it wide: one CTA per hidden row, its 8 warps taking the union's
+// codes in groups of 8 (one fp32 accumulator per code in registers).  Lane l
+// multiplies 16-byte bf16 vectors l, l+32, ... of the row and of the code's
+// embedding row (the union rows stay L2-resident across CTAs), and a fixed
+// butterfly finishes each dot product, so identical rows give bit-identical
+// logits.  z_U lives in shared memory; the CTA then takes lse_U and writes the
+// log-probability of each of the row's tokens.
 #include <cuda_bf16.h>
 
 #include "jet_internal.cuh"
@@ -21,23 +25,7 @@ namespace jet {
 namespace {
 
 constexpr int RT_THREADS = 256;   // 8 warps
-constexpr int RT_MAX_ROWS = 8;
-
-struct RtShape { int R, CH; size_t smem; };
-
-__host__ __device__ inline RtShape rt_shape(int d, int n_union) {
-  RtShape s;
-  const size_t row_bytes = (size_t)d * 2;
-  int R = RT_MAX_ROWS;
-  while (R > 1 && (size_t)R * (row_bytes + (size_t)n_union * 4) > 112 * 1024) --R;
-  int CH = (int)((64 * 1024) / row_bytes);
-  if (CH < 1) CH = 1;
-  if (CH > n_union) CH = n_union;
-  s.R = R;
-  s.CH = CH;
-  s.smem = (size_t)R * row_bytes + (size_t)CH * row_bytes + (size_t)R * n_union * 4;
-  return s;
-}
+constexpr int RT_GROUP = 8;       // codes per warp pass
 
 __device__ __forceinline__ float dot_bf16x8(uint4 h, uint4 w, float acc) {
   const __nv_bfloat162* hp = reinterpret_cast<const __nv_bfloat162*>(&h);
@@ -52,62 +40,71 @@ __device__ __forceinline__ float dot_bf16x8(uint4 h, uint4 w, float acc) {
   return acc;
 }
 
-__global__ void __launch_bounds__(RT_THREADS) restricted_kernel(const RestrictedArgs a, const RtShape sh) {
-  extern __shared__ __align__(16) uint8_t smem[];
+__global__ void __launch_bounds__(RT_THREADS) restricted_kernel(const RestrictedArgs a) {
+  __shared__ float sZ[JET_MAX_UNION];
+  __shared__ float sRed[2 * (RT_THREADS / 32)];
+  pdl_trigger();
+  pdl_wait();
   if (*(volatile const int*)a.err != 0) return;
-  const int d = a.d, U = a.n_union;
-  const int vec_per_row = d / 8;                       // 16-byte vectors per row
-  uint4* sH = reinterpret_cast<uint4*>(smem);                          // [R][d]
-  uint4* sW = sH + (size_t)sh.R * vec_per_row;                          // [CH][d]
-  float* sZ = reinterpret_cast<float*>(sW + (size_t)sh.CH * vec_per_row);   // [R][U]
+  const int r = blockIdx.x;
+  const int U = a.n_union;
+  const int nvec = a.d / 8;                             // 16-byte vectors per row
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r0 = blockIdx.x * sh.R;
-  const int nrows = min(sh.R, a.N - r0);
+  const uint4* h = reinterpret_cast<const uint4*>(a.H) + (size_t)r * nvec;
+  const uint4* Wv = reinterpret_cast<const uint4*>(a.W);
 
-  const uint4* Hg = reinterpret_cast<const uint4*>(a.H);
-  for (int i = threadIdx.x; i < nrows * vec_per_row; i += blockDim.x)
-    sH[i] = Hg[(size_t)r0 * vec_per_row + i];
-
-  const uint4* Wg = reinterpret_cast<const uint4*>(a.W);
-  for (int u0 = 0; u0 < U; u0 += sh.CH) {
-    const int nu = min(sh.CH, U - u0);
-    __syncthreads();
-    for (int i = threadIdx.x; i < nu * vec_per_row; i += blockDim.x) {
-      const int uu = i / vec_per_row, k = i - uu * vec_per_row;
-      sW[i] = Wg[(size_t)a.union_ids[u0 + uu] * vec_per_row + k];
-    }
-    __syncthreads();
-    for (int lr = warp; lr < nrows; lr += RT_THREADS / 32) {
-      const uint4* h = sH + (size_t)lr * vec_per_row;
-      for (int uu = 0; uu < nu; ++uu) {
-        const uint4* w = sW + (size_t)uu * vec_per_row;
-        float acc = 0.f;
-        for (int k = lane; k < vec_per_row; k += 32) acc = dot_bf16x8(h[k], w[k], acc);
+  for (int g0 = warp * RT_GROUP; g0 < U; g0 += RT_GROUP * (RT_THREADS / 32)) {
+    const int ng = min(RT_GROUP, U - g0);
+    const uint4* w[RT_GROUP];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        if (lane == 0) sZ[(size_t)lr * U + u0 + uu] = acc;
-      }
+    for (int i = 0; i < RT_GROUP; ++i)
+      w[i] = Wv + (size_t)a.union_ids[g0 + min(i, ng - 1)] * nvec;
+    float acc[RT_GROUP];
+#pragma unroll
+    for (int i = 0; i < RT_GROUP; ++i) acc[i] = 0.f;
+    for (int k = lane; k < nvec; k += 32) {
+      const uint4 hv = h[k];
+#pragma unroll
+      for (int i = 0; i < RT_GROUP; ++i) acc[i] = dot_bf16x8(hv, w[i][k], acc[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < RT_GROUP; ++i) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], o);
+    }
+    if (lane < ng) {
+      float v = acc[0];
+#pragma unroll
+      for (int i = 1; i < RT_GROUP; ++i) v = (lane == i) ? acc[i] : v;
+      sZ[g0 + lane] = v;
     }
   }
   __syncthreads();
 
-  for (int lr = warp; lr < nrows; lr += RT_THREADS / 32) {
-    const float* z = sZ + (size_t)lr * U;
-    float M = -INFINITY;
-    for (int u = lane; u < U; u += 32) M = fmaxf(M, z[u]);
+  // lse over the union: block max, then block sum of exp(z - max)
+  float M = -INFINITY;
+  for (int u = threadIdx.x; u < U; u += RT_THREADS) M = fmaxf(M, sZ[u]);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float s = 0.f;
-    for (int u = lane; u < U; u += 32) s += expf(z[u] - M);
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  if (lane == 0) sRed[warp] = M;
+  __syncthreads();
+  M = sRed[0];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    const float lse = M + logf(s);
-    const int r = r0 + lr;
-    if (lane == 0 && a.lse) a.lse[r] = lse;
-    for (int e = a.row_ptr[r] + lane; e < a.row_ptr[r + 1]; e += 32) {
-      const int j = a.row_list[e].y;
-      a.logp[j] = z[a.upos[j]] - lse;
-    }
+  for (int i = 1; i < RT_THREADS / 32; ++i) M = fmaxf(M, sRed[i]);
+  float sum = 0.f;
+  for (int u = threadIdx.x; u < U; u += RT_THREADS) sum += expf(sZ[u] - M);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  if (lane == 0) sRed[RT_THREADS / 32 + warp] = sum;
+  __syncthreads();
+  sum = 0.f;
+#pragma unroll
+  for (int i = 0; i < RT_THREADS / 32; ++i) sum += sRed[RT_THREADS / 32 + i];
+  const float lse = M + logf(sum);
+  if (threadIdx.x == 0 && a.lse) a.lse[r] = lse;
+  for (int e = a.row_ptr[r] + threadIdx.x; e < a.row_ptr[r + 1]; e += RT_THREADS) {
+    const int j = a.row_list[e].y;
+    a.logp[j] = sZ[a.upos[j]] - lse;
   }
 }
 
@@ -115,16 +112,7 @@ __global__ void __launch_bounds__(RT_THREADS) restricted_kernel(const Restricted
 
 cudaError_t launch_restricted(const RestrictedArgs& a, cudaStream_t st) {
   if (a.N <= 0) return cudaSuccess;
-  const RtShape sh = rt_shape(a.d, a.n_union);
-  static size_t configured = 0;
-  if (sh.smem > 48 * 1024 && sh.smem > configured) {
-    cudaError_t e = cudaFuncSetAttribute(restricted_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)sh.smem);
-    if (e != cudaSuccess) return e;
-    configured = sh.smem;
-  }
-  restricted_kernel<<<(a.N + sh.R - 1) / sh.R, RT_THREADS, sh.smem, st>>>(a, sh);
-  return cudaGetLastError();
+  return launch_dependent(restricted_kernel, dim3(a.N), dim3(RT_THREADS), 0, st, a);
 }
 
 }  // namespace jet

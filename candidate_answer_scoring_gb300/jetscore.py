@@ -74,6 +74,7 @@ def load() -> C.CDLL:
     lib.jet_plan_info.argtypes = [P, I, C.POINTER(C.c_int)]
     lib.jet_profile_enable.argtypes = [P, I]
     lib.jet_profile_read.argtypes = [P, C.POINTER(C.c_double), I]
+    lib.jet_selftest_wait_timeout.argtypes = [P, I, P]
     _lib = lib
     return lib
 
@@ -205,6 +206,10 @@ class JetScorer:
         res = {k: {"launches": int(out[2 * i]), "ms": float(out[2 * i + 1])} for i, k in enumerate(self.KERNELS)}
         res["untimed_launches"] = int(out[10])
         return res
+
+    def selftest_wait_timeout(self, limit_us: int) -> int:
+        """Run the bounded-wait diagnostic; returns the status (JET_ERR_TIMEOUT expected)."""
+        return self.lib.jet_selftest_wait_timeout(self._h, int(limit_us), _stream(self.device))
 
     def sync_status(self) -> int:
         return self.lib.jet_sync_status(self._h, _stream(self.device))

@@ -200,6 +200,17 @@ int jet_profile_enable(jet_ctx *ctx, int enable);
 int jet_profile_read(jet_ctx *ctx, double *out, int n_out);
 
 /*
+ * jet_selftest_wait_timeout: diagnostic of the library's failure handling.
+ * Launches one CTA that waits, with the same bounded wait every kernel of the
+ * library uses, on a barrier that nothing completes, giving up after
+ * limit_us microseconds (1 .. 2,000,000).  Returns JET_ERR_TIMEOUT when the
+ * wait ran out and reported itself through the context's error word as
+ * designed (the expected result), JET_ERR_CUDA otherwise.  The context stays
+ * usable afterwards.
+ */
+int jet_selftest_wait_timeout(jet_ctx *ctx, int limit_us, void *cuda_stream);
+
+/*
  * jet_score_tokens_noalloc: the computation of jet_score_tokens (one scored
  * token per row, logp[i] = z[i, tok_ids[i]] - lse[i]) for callers that cannot
  * allocate device memory -- code running inside a process whose device memory
