@@ -15,29 +15,47 @@ using namespace jet;
 namespace jet {
 
 // Choose the number of vocabulary splits S per row tile: every unit is one row
-// tile over n_vt/S vocabulary tiles, units run G at a time, so the busiest CTA
-// processes ceil(n_mt*S/G) * ceil(n_vt/S) tiles; take the smallest such count
-// (ties: fewer splits).  Bands of Gm row tiles keep Gm H tiles (128*d*2 bytes
-// each) within ~48 MB of L2 while the band's units stream W.
-Plan make_plan(int N, int V, int d, int G, int units_cap) {
+// tile over n_vt/S vocabulary tiles, G_u units run at a time (G SMs, or G/2
+// CTA pairs), so the busiest CTA processes ceil(n_mt*S/G_u) * ceil(n_vt/S)
+// tiles; take the smallest such count (ties: fewer splits).  Bands of Gm row
+// tiles keep Gm H tiles (rows*d*2 bytes each) within ~48 MB of L2 while the
+// band's units stream W.
+Plan make_plan(int N, int V, int d, int G, int units_cap, bool pair) {
   Plan p;
-  p.n_mt = (N + BM - 1) / BM;
+  p.pair = pair ? 1 : 0;
+  const int rows = plan_tile_rows(p);
+  const int per_unit = 1 + p.pair;                 // CTAs per unit
+  const int G_u = std::max(1, G / per_unit);
+  p.n_mt = (N + rows - 1) / rows;
   p.n_vt = (V + BN - 1) / BN;
-  const int S_max = std::max(1, std::min(p.n_vt, units_cap / std::max(1, p.n_mt)));
+  const int S_max = std::max(1, std::min(p.n_vt, units_cap / (per_unit * std::max(1, p.n_mt))));
   long long best = -1;
   for (int S = 1; S <= S_max; ++S) {
-    const long long waves = ((long long)p.n_mt * S + G - 1) / G;
+    const long long waves = ((long long)p.n_mt * S + G_u - 1) / G_u;
     const long long t = waves * ((p.n_vt + S - 1) / S);
     if (best < 0 || t < best) { best = t; p.S = S; }
   }
-  const long long a_tile = (long long)BM * d * 2;
+  const long long a_tile = (long long)rows * d * 2;
   const int gm_max = (int)std::max(1LL, (48LL << 20) / a_tile);
   p.Gm = std::max(1, std::min(p.n_mt, gm_max));
   p.n_full_bands = p.n_mt / p.Gm;
   p.r_last = p.n_mt - p.n_full_bands * p.Gm;
   p.units = p.n_mt * p.S;
-  p.grid = std::min(p.units, G);
+  p.grid = per_unit * std::min(p.units, G_u);
   return p;
+}
+
+// The paired head serves every batch of more than one 128-row tile: it halves
+// each CTA's share of the W tile, which keeps twice the W bytes in flight per
+// SM.  JETSCORE_HEAD_PAIR=0/1 forces a variant (diagnostics).
+bool head_use_pair(int N) {
+  static int env = -2;
+  if (env == -2) {
+    const char* v = std::getenv("JETSCORE_HEAD_PAIR");
+    env = v ? std::atoi(v) : -1;
+  }
+  if (env >= 0) return env != 0;
+  return N > BM;
 }
 
 int head_prefetch_kblocks(const Plan& p) {
@@ -167,7 +185,7 @@ int encode_kmajor(jet_ctx* c, CUtensorMap* map, const void* base, int rows, int 
 
 const Plan& plan_for(jet_ctx* c, int n_rows) {
   if (c->plan_rows != n_rows) {
-    c->plan = make_plan(n_rows, c->V, c->d, c->num_sms, c->units_cap);
+    c->plan = make_plan(n_rows, c->V, c->d, c->num_sms, c->units_cap, head_use_pair(n_rows));
     c->plan_rows = n_rows;
   }
   return c->plan;
@@ -176,16 +194,17 @@ const Plan& plan_for(jet_ctx* c, int n_rows) {
 // Full-vocabulary log-probabilities for the rows/tokens the pre-pass listed.
 int run_full_head(jet_ctx* c, const void* H, const void* W, int n_rows, float* logp, float* lse,
                   cudaStream_t st) {
+  const Plan& plan = plan_for(c, n_rows);
   CUtensorMap tmH, tmW;
   int rc = encode_kmajor(c, &tmH, H, n_rows, BM);
   if (rc != JET_OK) return rc;
-  rc = encode_kmajor(c, &tmW, W, c->V, BN);
+  rc = encode_kmajor(c, &tmW, W, c->V, plan.pair ? HeadShape<true>::B_ROWS : HeadShape<false>::B_ROWS);
   if (rc != JET_OK) return rc;
   HeadArgs ha;
   ha.N = n_rows;
   ha.V = c->V;
   ha.d = c->d;
-  ha.plan = plan_for(c, n_rows);
+  ha.plan = plan;
   ha.row_ptr = c->row_ptr;
   ha.row_list = c->row_list;
   ha.zg = c->zg;
@@ -462,7 +481,7 @@ int jet_selftest_wait_timeout(jet_ctx* c, int limit_us, void* stream) {
 int jet_plan_info(jet_ctx* c, int n_rows, int* info) {
   if (!c || !info || n_rows < 1 || n_rows > c->max_rows) return JET_ERR_ARG;
   const Plan& p = plan_for(c, n_rows);
-  const int v[8] = {p.n_mt, p.n_vt, p.S, p.Gm, p.units, p.grid, BM, BN};
+  const int v[8] = {p.n_mt, p.n_vt, p.S, p.Gm, p.units, p.grid, plan_tile_rows(p), BN};
   std::memcpy(info, v, sizeof v);
   return JET_OK;
 }

@@ -9,18 +9,27 @@
 
 namespace jet {
 
-// ---- full-vocabulary head tile shape (tcgen05, cta_group::1) ---------------
-constexpr int BM = 128;             // hidden rows per tile = TMEM lanes
+// ---- full-vocabulary head tile shape (tcgen05) ------------------------------
+// One CTA owns 128 hidden rows (its TMEM lanes) and 256 vocabulary columns of
+// a tile.  In the paired variant two CTAs of a cluster run one
+// tcgen05.mma.cta_group::2 (M = 256): each stages its own 128 rows of H and
+// half (128 rows) of the W tile.
+constexpr int BM = 128;             // hidden rows per CTA tile = TMEM lanes
 constexpr int BN = 256;             // vocabulary columns per tile = fp32 TMEM columns
 constexpr int BK = 64;              // bf16 elements per k-block = one 128-byte swizzle row
-constexpr int STAGES = 4;           // shared-memory pipeline depth
 constexpr int EPI_WARPS = 8;        // two warpgroups: column halves of a tile
 constexpr int HEAD_THREADS = (2 + EPI_WARPS) * 32;
-constexpr int A_STAGE_BYTES = BM * BK * 2;
-constexpr int B_STAGE_BYTES = BN * BK * 2;
-constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
-constexpr int HEAD_SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 constexpr int TMEM_COLS = 2 * BN;   // two accumulators (double buffer)
+
+template <bool PAIR>
+struct HeadShape {
+  static constexpr int B_ROWS = PAIR ? BN / 2 : BN;   // W rows this CTA stages per tile
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = B_ROWS * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = PAIR ? 6 : 4;          // shared-memory ring depth
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+};
 
 // Device-side error word layout: err[0] = first status (0 = ok),
 // err[1] = index of the offending element, err[2] = where a wait gave up.
@@ -60,12 +69,22 @@ cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, si
 }
 
 // Vocabulary-split schedule of the head: unit u = (row tile m, split s) covers
-// vocabulary tiles [s*n_vt/S, (s+1)*n_vt/S).  Units are ordered band by band
-// (Gm row tiles per band), split-major inside a band, so CTAs running together
-// share W tiles through L2 while the band's H tiles stay L2-resident.
+// vocabulary tiles [s*n_vt/S, (s+1)*n_vt/S).  A row tile is 128 rows (one CTA)
+// or, paired, 256 rows (a CTA pair).  Units are ordered band by band (Gm row
+// tiles per band), split-major inside a band, so CTAs running together share
+// W tiles through L2 while the band's H tiles stay L2-resident.
 struct Plan {
   int n_mt = 0, n_vt = 0, S = 1, Gm = 1, n_full_bands = 0, r_last = 0, units = 0, grid = 0;
+  int pair = 0;   // 1: units run on CTA pairs (cta_group::2)
 };
+
+__host__ __device__ __forceinline__ int plan_tile_rows(const Plan& p) { return p.pair ? 2 * BM : BM; }
+
+// Slot of the (max, sum-exp) partial of (unit u, CTA sub of the pair, column
+// half h, row lr of the CTA's 128).
+__host__ __device__ __forceinline__ size_t part_slot(const Plan& p, int u, int sub, int h, int lr) {
+  return (((size_t)u * (1 + p.pair) + sub) * 2 + h) * BM + lr;
+}
 
 struct HeadArgs {
   int N, V, d;
@@ -73,13 +92,16 @@ struct HeadArgs {
   const int* row_ptr;   // [N+1]   CSR over rows of the scored tokens
   const int2* row_list; // [n_tok] (token id, token index), sorted by id within a row
   float* zg;            // [n_tok] gathered logit of each scored token
-  float2* part;         // [units*2*BM] per (unit, column half, row): (max, sum exp(z - max))
+  float2* part;         // per (unit, CTA of the pair, column half, row): (max, sum exp(z - max))
   int* err;
   int pf_kblocks;       // L2 prefetch distance for W, in k-blocks of the CTA's stream (0: off)
 };
 
-// Host: schedule for N rows with at most units_cap units on G SMs.
-Plan make_plan(int N, int V, int d, int G, int units_cap);
+// Host: schedule for N rows on G SMs; units * (1 + pair) <= units_cap.
+Plan make_plan(int N, int V, int d, int G, int units_cap, bool pair);
+
+// Host: whether the paired (2-SM) head serves N rows.
+bool head_use_pair(int N);
 
 // Host: L2 prefetch distance (k-blocks) for the head's W stream.  Off by
 // default: measured on GB300 it slowed the W-streaming head (two CTAs share
@@ -128,6 +150,7 @@ struct PrepArgs {
 };
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t st);
 
+// tmW's box must have HeadShape<a.plan.pair>::B_ROWS rows; tmH's box BM rows.
 cudaError_t launch_head(const CUtensorMap& tmH, const CUtensorMap& tmW, const HeadArgs& a,
                         cudaStream_t st);
 

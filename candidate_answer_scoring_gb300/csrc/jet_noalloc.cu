@@ -130,8 +130,10 @@ extern "C" int jet_score_tokens_noalloc(const void* H, const void* W, int d, int
   pa.err = err;
   if (launch_prep(pa, st) != cudaSuccess) return JET_ERR_CUDA;
 
+  const Plan plan = make_plan(n_pos, V, d, sms, NA_MAX_UNITS, head_use_pair(n_pos));
   CUtensorMap tmH, tmW;
-  if (encode(&tmH, H, d, n_pos, BM) != JET_OK || encode(&tmW, W, d, V, BN) != JET_OK) {
+  if (encode(&tmH, H, d, n_pos, BM) != JET_OK ||
+      encode(&tmW, W, d, V, plan.pair ? HeadShape<true>::B_ROWS : HeadShape<false>::B_ROWS) != JET_OK) {
     cudaStreamSynchronize(st);
     return JET_ERR_CUDA;
   }
@@ -139,7 +141,7 @@ extern "C" int jet_score_tokens_noalloc(const void* H, const void* W, int d, int
   ha.N = n_pos;
   ha.V = V;
   ha.d = d;
-  ha.plan = make_plan(n_pos, V, d, sms, NA_MAX_UNITS);
+  ha.plan = plan;
   ha.row_ptr = row_ptr;
   ha.row_list = row_list;
   ha.zg = zg;

@@ -7,19 +7,30 @@
 // split ("JET: Justification Evaluation in Transformer", Eq. 1-2: the
 // denominator runs over the full vocabulary; GPU scoring computes it but
 // transfers only the candidate log-probabilities).  The [N, V] logit matrix
-// lives only in tensor memory, one 128 x 256 fp32 tile at a time.
+// lives only in tensor memory, one 128 x 256 fp32 tile per CTA at a time.
 //
-// Structure (one persistent CTA per SM, 320 threads):
+// Structure (persistent CTAs, 320 threads each):
 //   warp 0      TMA producer: H and W k-blocks (64 bf16 = 128 B, 128B swizzle)
-//               into a 4-stage shared-memory ring, completion on mbarriers;
+//               into a shared-memory ring, completion on mbarriers;
 //   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators) and
-//               issues tcgen05.mma (M=128, N=256, K=16) from one thread;
+//               issues tcgen05.mma (K=16 per instruction) from one thread;
 //   warps 2-9   epilogue: each thread owns one row (its TMEM lane) and half of
 //               the tile's columns, reads them with tcgen05.ld, folds them into
 //               a running (max, sum-exp) and picks out the logits of its row's
 //               tokens while walking the row's sorted token list.
 // The two accumulators let the epilogue of tile j overlap the MMAs of tile
-// j+1.  Every mbarrier wait is bounded: on timeout the kernel records
+// j+1.
+//
+// Paired variant (PAIR = true, clusters of two CTAs on two SMs): one
+// tcgen05.mma.cta_group::2 computes a 256 x 256 tile; each CTA stages its own
+// 128 rows of H and 128 of the tile's 256 W rows, so its 6-stage ring holds
+// twice the W bytes of the single-CTA ring.  This is what lets few rows
+// (N ~ 256, where two row tiles would otherwise share each W tile and halve
+// each CTA's DRAM bytes in flight) stream W at full bandwidth.  Both CTAs'
+// TMA copies complete on the issuing CTA's barrier, which expects the bytes of
+// both halves, and the MMA commits are multicast back to both CTAs.
+//
+// Every mbarrier wait is bounded: on timeout the kernel records
 // JET_ERR_TIMEOUT, drains its own copies and MMAs, frees TMEM and returns.
 #include <climits>
 
@@ -29,7 +40,8 @@
 namespace jet {
 namespace {
 
-constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;   // 2 s per wait
+constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;        // 2 s per wait
+constexpr unsigned long long EXIT_LIMIT_NS = 3 * WAIT_LIMIT_NS;    // pair exit handshake
 
 // ---- TMA ----------------------------------------------------------------------
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
@@ -37,6 +49,16 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+      : "memory");
+}
+
+// Paired form: the copy lands in this CTA's shared memory and completes on
+// the barrier at cluster address `bar` (the issuing CTA's barrier).
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
       : "memory");
 }
 
@@ -48,12 +70,66 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x
                : "memory");
 }
 
+// ---- cluster ------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Cluster address of the object at the same shared-memory offset in CTA `rank`.
+__device__ __forceinline__ uint32_t cluster_addr(const void* local, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  return remote;
+}
+
+// Arrive on the mbarrier at the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ void mbar_arrive_cluster(uint64_t* bar_local, uint32_t rank) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr(bar_local, rank))
+               : "memory");
+}
+
+// Spin on %globaltimer for about `ns` nanoseconds.
+__device__ __forceinline__ void settle_ns(unsigned long long ns) {
+  const unsigned long long t0 = globaltimer();
+  while (globaltimer() - t0 < ns) {
+  }
+}
+
 // ---- tcgen05 ------------------------------------------------------------------
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+template <bool PAIR>
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+  if constexpr (PAIR) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  } else {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+}
+
+template <bool PAIR>
+__device__ __forceinline__ void tmem_dealloc(uint32_t base, uint32_t ncols) {
+  if constexpr (PAIR)
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(base), "r"(ncols) : "memory");
+  else
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(base), "r"(ncols) : "memory");
 }
 
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
@@ -69,26 +145,63 @@ __device__ __forceinline__ uint64_t sdesc_k128(uint32_t saddr) {
 }
 
 // Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major,
-// N = BN, M = BM.
-constexpr uint32_t IDESC = (1u << 4)                 // D format: f32
-                           | (1u << 7)               // A format: bf16
-                           | (1u << 10)              // B format: bf16
-                           | ((uint32_t)(BN >> 3) << 17)
-                           | ((uint32_t)(BM >> 4) << 24);
-
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accum) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(IDESC), "r"(accum)
-      : "memory");
+// N = BN, M = 128 (one CTA) or 256 (CTA pair).
+template <bool PAIR>
+__host__ __device__ constexpr uint32_t idesc() {
+  return (1u << 4)                                   // D format: f32
+         | (1u << 7)                                 // A format: bf16
+         | (1u << 10)                                // B format: bf16
+         | ((uint32_t)(BN >> 3) << 17)               // N >> 3
+         | ((uint32_t)((PAIR ? 2 * BM : BM) >> 4) << 24);   // M >> 4
 }
 
-__device__ __forceinline__ void tc_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   smem_u32(bar))
-               : "memory");
+template <bool PAIR>
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accum) {
+  if constexpr (PAIR)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc<true>()), "r"(accum)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc<false>()), "r"(accum)
+        : "memory");
+}
+
+// Arrive on `bar` once every MMA issued so far by this thread has completed:
+// in the paired variant on the barrier at that offset in both CTAs.
+template <bool PAIR>
+__device__ __forceinline__ void tc_commit_all(uint64_t* bar) {
+  if constexpr (PAIR) {
+    const uint16_t mask = 0x3;
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"(mask)
+        : "memory");
+  } else {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+  }
+}
+
+// As tc_commit_all, but only on this CTA's barrier.
+template <bool PAIR>
+__device__ __forceinline__ void tc_commit_local(uint64_t* bar) {
+  if constexpr (PAIR)
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+  else
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
 }
 
 // Load 32 consecutive fp32 columns of this thread's TMEM lane, then wait for
@@ -124,44 +237,51 @@ __device__ __forceinline__ float ex2(float x) {   // hardware 2^x (MUFU), flushe
 
 constexpr float LOG2E = 1.4426950408889634f;
 
+template <bool PAIR>
 __global__ void __launch_bounds__(HEAD_THREADS, 1)
     head_lse_gather_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmW,
                            const HeadArgs a) {
+  using SH = HeadShape<PAIR>;
+  constexpr int NST = SH::STAGES;
   extern __shared__ uint8_t smem_raw[];
   // 128B-swizzled operand tiles must start on 1024-byte boundaries
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
-  uint8_t* sB = smem + STAGES * A_STAGE_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * B_STAGE_BYTES);
-  uint64_t* full = bars;                  // [STAGES] TMA -> MMA
-  uint64_t* empty = bars + STAGES;        // [STAGES] MMA -> TMA
-  uint64_t* tfull = bars + 2 * STAGES;    // [2] MMA -> epilogue
-  uint64_t* tempty = tfull + 2;           // [2] epilogue -> MMA
+  uint8_t* sB = smem + NST * SH::A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + NST * SH::B_BYTES);
+  uint64_t* full = bars;                  // [NST] TMA -> MMA (paired: used in the issuing CTA)
+  uint64_t* empty = bars + NST;           // [NST] MMA -> TMA
+  uint64_t* tfull = bars + 2 * NST;       // [2] MMA -> epilogue
+  uint64_t* tempty = tfull + 2;           // [2] epilogue(s) -> MMA
   uint64_t* drain = tempty + 2;           // [1] MMA drain on abort
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* exitb = drain + 1;            // [1] paired exit handshake
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(exitb + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = PAIR ? cluster_rank() : 0u;   // CTA within the pair; 0 issues the MMAs
+  const bool issuer = rank == 0;
+  const int unit0 = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int unit_step = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
   pdl_trigger();   // the merge kernel may be scheduled; it waits for this grid to finish
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < STAGES; ++i) {
-      mbar_init(&full[i], 1);
+    for (int i = 0; i < NST; ++i) {
+      mbar_init(&full[i], 1);   // the issuer's arrive.expect_tx (+ both CTAs' bytes when paired)
       mbar_init(&empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], EPI_WARPS);
+      mbar_init(&tempty[i], EPI_WARPS * (PAIR ? 2 : 1));
     }
     mbar_init(drain, 1);
+    mbar_init(exitb, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  if constexpr (PAIR) cluster_sync_all();   // peer barriers exist before any remote arrival
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                 "r"(TMEM_COLS)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    tmem_alloc<PAIR>(tmem_slot, TMEM_COLS);
     tc_fence_before();
   }
   __syncthreads();
@@ -169,6 +289,7 @@ __global__ void __launch_bounds__(HEAD_THREADS, 1)
   const uint32_t tmem_base = *tmem_slot;
   const Plan& P = a.plan;
   const int kblocks = a.d / BK;
+  const int tile_rows = plan_tile_rows(P);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -177,48 +298,63 @@ __global__ void __launch_bounds__(HEAD_THREADS, 1)
       uint32_t phase = 0;
       uint32_t issued_mask = 0, issued_parity = 0;   // per stage: has a load, parity of its phase
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < P.units; u += gridDim.x) {
+      for (int u = unit0; ok && u < P.units; u += unit_step) {
         int m, vt0, vt1;
         plan_unit(P, u, m, vt0, vt1);
+        const int a_row = m * tile_rows + (int)rank * BM;
         for (int vt = vt0; ok && vt < vt1; ++vt) {
           if (*abort_flag) { ok = false; break; }
+          const int b_row = vt * BN + (int)rank * SH::B_ROWS;
           for (int kb = 0; kb < kblocks; ++kb) {
             if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.err, 1, WAIT_LIMIT_NS)) { ok = false; break; }
-            mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
-            tma_load_2d(sA + stage * A_STAGE_BYTES, &tmH, kb * BK, m * BM, &full[stage]);
-            tma_load_2d(sB + stage * B_STAGE_BYTES, &tmW, kb * BK, vt * BN, &full[stage]);
-            if (a.pf_kblocks > 0) {   // keep more W bytes in flight to DRAM than the ring holds
+            if constexpr (PAIR) {
+              if (issuer) mbar_arrive_expect_tx(&full[stage], 2 * SH::STAGE_BYTES);   // both CTAs' halves
+              const uint32_t bar = cluster_addr(&full[stage], 0);
+              tma_load_2d_pair(sA + stage * SH::A_BYTES, &tmH, kb * BK, a_row, bar);
+              tma_load_2d_pair(sB + stage * SH::B_BYTES, &tmW, kb * BK, b_row, bar);
+            } else {
+              mbar_arrive_expect_tx(&full[stage], SH::STAGE_BYTES);
+              tma_load_2d(sA + stage * SH::A_BYTES, &tmH, kb * BK, a_row, &full[stage]);
+              tma_load_2d(sB + stage * SH::B_BYTES, &tmW, kb * BK, b_row, &full[stage]);
+            }
+            if (a.pf_kblocks > 0) {   // optional: more W bytes in flight than the ring holds
               const int ip = (vt - vt0) * kblocks + kb + a.pf_kblocks;
               const int vtp = vt0 + ip / kblocks;
-              if (vtp < vt1) tma_prefetch_l2_2d(&tmW, (ip % kblocks) * BK, vtp * BN);
+              if (vtp < vt1) tma_prefetch_l2_2d(&tmW, (ip % kblocks) * BK, vtp * BN + (int)rank * SH::B_ROWS);
             }
             issued_mask |= 1u << stage;
             issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            if (++stage == NST) { stage = 0; phase ^= 1u; }
           }
         }
       }
       if (ok) {
         // tail: wait until the MMA has released every stage, so that no
         // barrier arrival is still pending when the CTA exits
-        for (int i = 0; i < STAGES; ++i) {
+        for (int i = 0; i < NST; ++i) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.err, 5, WAIT_LIMIT_NS)) break;
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          if (++stage == NST) { stage = 0; phase ^= 1u; }
         }
-      } else {
+      } else if (!PAIR || issuer) {
         // abort: let copies already in flight land before the CTA exits
         volatile int never = 0;
-        for (int s = 0; s < STAGES; ++s)
-          if (issued_mask & (1u << s)) mbar_wait(&full[s], (issued_parity >> s) & 1u, &never, nullptr, 0, WAIT_LIMIT_NS);
+        for (int s = 0; s < NST; ++s)
+          if (issued_mask & (1u << s))
+            mbar_wait(&full[s], (issued_parity >> s) & 1u, &never, nullptr, 0, WAIT_LIMIT_NS);
+      } else {
+        // abort in the second CTA: its copies complete on the issuer's barrier,
+        // which it cannot observe; give them ample time (a TMA round trip is
+        // microseconds) before the exit handshake lets the pair leave
+        settle_ns(200000ull);
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && issuer) {
+      // ------------------------------------------------------------ MMA issuer
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true, any = false;
-      for (int u = blockIdx.x; ok && u < P.units; u += gridDim.x) {
+      for (int u = unit0; ok && u < P.units; u += unit_step) {
         int m, vt0, vt1;
         plan_unit(P, u, m, vt0, vt1);
         for (int vt = vt0; ok && vt < vt1; ++vt) {
@@ -228,24 +364,24 @@ __global__ void __launch_bounds__(HEAD_THREADS, 1)
           for (int kb = 0; kb < kblocks; ++kb) {
             if (!mbar_wait(&full[stage], phase, abort_flag, a.err, 3, WAIT_LIMIT_NS)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t a0 = smem_u32(sA + stage * A_STAGE_BYTES);
-            const uint32_t b0 = smem_u32(sB + stage * B_STAGE_BYTES);
+            const uint32_t a0 = smem_u32(sA + stage * SH::A_BYTES);
+            const uint32_t b0 = smem_u32(sB + stage * SH::B_BYTES);
 #pragma unroll
             for (int k = 0; k < BK / 16; ++k)   // 16 bf16 = 32 bytes along K per MMA
-              tc_mma(d_tmem, sdesc_k128(a0 + 32 * k), sdesc_k128(b0 + 32 * k), (kb | k) != 0);
-            tc_commit(&empty[stage]);
+              tc_mma<PAIR>(d_tmem, sdesc_k128(a0 + 32 * k), sdesc_k128(b0 + 32 * k), (kb | k) != 0);
+            tc_commit_all<PAIR>(&empty[stage]);
             any = true;
-            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            if (++stage == NST) { stage = 0; phase ^= 1u; }
           }
           if (!ok) break;
-          tc_commit(&tfull[acc]);
+          tc_commit_all<PAIR>(&tfull[acc]);
           acc ^= 1;
           if (acc == 0) acc_phase ^= 1u;
         }
       }
       if (!ok && any) {   // wait until every MMA issued so far has completed
         volatile int never = 0;
-        tc_commit(drain);
+        tc_commit_local<PAIR>(drain);
         mbar_wait(drain, 0, &never, nullptr, 0, WAIT_LIMIT_NS);
       }
     }
@@ -259,10 +395,10 @@ __global__ void __launch_bounds__(HEAD_THREADS, 1)
     pdl_wait();   // row lists and the error word come from the pre-pass
     bool ok = *(volatile const int*)a.err == 0;
     if (!ok) *abort_flag = 1;   // pre-pass rejected the batch: every role stops
-    for (int u = blockIdx.x; ok && u < P.units; u += gridDim.x) {
+    for (int u = unit0; ok && u < P.units; u += unit_step) {
       int m, vt0, vt1;
       plan_unit(P, u, m, vt0, vt1);
-      const int row = m * BM + row_in_tile;
+      const int row = m * tile_rows + (int)rank * BM + row_in_tile;
       const bool valid = row < a.N;
       int e = 0, e_end = 0, t_next = INT_MAX;
       if (valid) {
@@ -318,36 +454,73 @@ __global__ void __launch_bounds__(HEAD_THREADS, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[acc]);
+        if (lane == 0) {
+          if (PAIR && !issuer) mbar_arrive_cluster(&tempty[acc], 0);
+          else mbar_arrive(&tempty[acc]);
+        }
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
       }
-      if (ok && valid) a.part[((size_t)u * 2 + half) * BM + row_in_tile] = make_float2(m_run, s_run);
+      if (ok && valid) a.part[part_slot(P, u, (int)rank, half, row_in_tile)] = make_float2(m_run, s_run);
     }
   }
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) {
+    // neither CTA of the pair leaves while the other may still signal it or
+    // read its shared memory through the MMA
+    if (threadIdx.x == 0) {
+      mbar_arrive_cluster(exitb, rank ^ 1u);
+      volatile int never = 0;
+      mbar_wait(exitb, 0, &never, a.err, 7, EXIT_LIMIT_NS);
+    }
+    __syncthreads();
+  }
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
-                 : "memory");
+    tmem_dealloc<PAIR>(tmem_base, TMEM_COLS);
   }
+}
+
+template <bool PAIR>
+cudaError_t launch_variant(const CUtensorMap& tmH, const CUtensorMap& tmW, const HeadArgs& a, cudaStream_t st) {
+  static bool configured = false;   // per process; the attribute is per function
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(head_lse_gather_kernel<PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         HeadShape<PAIR>::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.plan.grid);
+  cfg.blockDim = dim3(HEAD_THREADS);
+  cfg.dynamicSmemBytes = HeadShape<PAIR>::SMEM_BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (pdl_enabled()) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (PAIR) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = 2;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, head_lse_gather_kernel<PAIR>, tmH, tmW, a);
 }
 
 }  // namespace
 
 cudaError_t launch_head(const CUtensorMap& tmH, const CUtensorMap& tmW, const HeadArgs& a, cudaStream_t st) {
-  static bool configured = false;   // per process; the attribute is per function
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(head_lse_gather_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         HEAD_SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
-  return launch_dependent(head_lse_gather_kernel, dim3(a.plan.grid), dim3(HEAD_THREADS), HEAD_SMEM_BYTES, st, tmH,
-                          tmW, a);
+  return a.plan.pair ? launch_variant<true>(tmH, tmW, a, st) : launch_variant<false>(tmH, tmW, a, st);
 }
 
 }  // namespace jet

@@ -29,22 +29,23 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeArgs a) {
   pdl_wait();
   if (*(volatile const int*)a.err != 0 || r >= a.N) return;
   const Plan& P = a.plan;
-  const int m_tile = r / BM, lr = r - m_tile * BM;
+  const int rows = plan_tile_rows(P);
+  const int m_tile = r / rows, sub = (r - m_tile * rows) / BM, lr = r % BM;
   float m = -INFINITY, s = 0.f;
-  const int n_slots = 2 * P.S;
+  const int n_slots = 2 * P.S;                        // (split, column half) pairs
   int slot = lane;
   for (; slot + 96 < n_slots; slot += 128) {        // four independent loads in flight
     float2 p[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int sl = slot + 32 * i;
-      p[i] = a.part[((size_t)plan_unit_of(P, m_tile, sl >> 1) * 2 + (sl & 1)) * BM + lr];
+      p[i] = a.part[part_slot(P, plan_unit_of(P, m_tile, sl >> 1), sub, sl & 1, lr)];
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) lse_fold(m, s, p[i].x, p[i].y);
   }
   for (; slot < n_slots; slot += 32) {
-    const float2 p = a.part[((size_t)plan_unit_of(P, m_tile, slot >> 1) * 2 + (slot & 1)) * BM + lr];
+    const float2 p = a.part[part_slot(P, plan_unit_of(P, m_tile, slot >> 1), sub, slot & 1, lr)];
     lse_fold(m, s, p.x, p.y);
   }
 #pragma unroll
