@@ -187,6 +187,16 @@ def time_oracle(steps_wl, n_sets, repeats=1):
     return dt, subs[0].n_tok, oracle.max_threads()
 
 
+def cpu_sample_sets(steps_wl, n_total, target_s):
+    """Number of leading sets whose oracle run takes about target_s seconds of
+    wall time on this host (the oracle runs rows in parallel, so the probe
+    uses one set per thread)."""
+    import oracle
+    probe = max(1, min(n_total, oracle.max_threads()))
+    dt, _, _ = time_oracle(steps_wl, probe)
+    return max(1, min(n_total, int(probe * target_s / max(dt, 1e-4))))
+
+
 def reference_arm(args, world, rank):
     if rank != 0:
         return 0
@@ -195,14 +205,11 @@ def reference_arm(args, world, rank):
     import oracle
     oracle.build()
     # size one step to about 2 s of oracle work, then cap the whole run at ~3 min
-    probe_sets = 1
-    dt1, _, _ = time_oracle(steps_wl, probe_sets)
-    per_set = max(dt1 / probe_sets, 1e-4)
-    n_sets = max(1, min(wl.n_sets, int(2.0 / per_set)))
+    n_sets = cpu_sample_sets(steps_wl, wl.n_sets, target_s=2.0)
     K = args.steps if args.steps is not None else 5
     W = args.warmup if args.warmup is not None else 1
     budget = 180.0
-    step_est = per_set * n_sets
+    step_est = 2.0
     k_run = max(1, min(K, int(budget / max(step_est, 1e-3)) - W))
     for _ in range(W):
         time_oracle(steps_wl, n_sets)
@@ -412,8 +419,7 @@ def gpu_arm(args, world, rank, local):
     if world == 1 and not args.no_cpu_baseline:
         import oracle
         oracle.build()
-        dt1, _, _ = time_oracle(steps_wl, 1)
-        n_sets = max(1, min(wl.n_sets, int(15.0 / max(dt1, 1e-4))))
+        n_sets = cpu_sample_sets(steps_wl, wl.n_sets, target_s=15.0)
         dt, ntok, threads = time_oracle(steps_wl, n_sets)
         line["cpu_baseline"] = {
             "value": ntok / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
