@@ -27,8 +27,9 @@ struct HeadShape {
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = B_ROWS * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = PAIR ? 6 : 4;          // shared-memory ring depth
+  static constexpr int STAGES = PAIR ? 6 : 4;          // shared-memory ring depth (7 measured no faster)
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 };
 
 // Device-side error word layout: err[0] = first status (0 = ok),

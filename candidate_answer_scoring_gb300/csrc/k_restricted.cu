@@ -10,12 +10,12 @@
 // cancels and q = softmax(z / T) over the set's codes (step 6).
 //
 // Work is tiny (|U| is tens of codes) and latency-bound, so the kernel
-// spreads it wide: one CTA per hidden row, its 8 warps taking the union's
-// codes in groups of 8 (one fp32 accumulator per code in registers).  Lane l
-// multiplies 16-byte bf16 vectors l, l+32, ... of the row and of the code's
-// embedding row (the union rows stay L2-resident across CTAs), and a fixed
-// butterfly finishes each dot product, so identical rows give bit-identical
-// logits.  z_U lives in shared memory; the CTA then takes lse_U and writes the
+// spreads it wide: one CTA of 32 warps per hidden row, one code per warp at a
+// time.  Lane l multiplies 16-byte bf16 vectors l, l+32, ... of the row and
+// of the code's embedding row (the union rows stay L2-resident across CTAs),
+// loading up to 4 vector pairs before using them, and a fixed butterfly
+// finishes each dot product, so identical rows give bit-identical logits.
+// z_U lives in shared memory; the CTA then takes lse_U and writes the
 // log-probability of each of the row's tokens.
 #include <cuda_bf16.h>
 
@@ -24,8 +24,9 @@
 namespace jet {
 namespace {
 
-constexpr int RT_THREADS = 256;   // 8 warps
-constexpr int RT_GROUP = 8;       // codes per warp pass
+constexpr int RT_THREADS = 1024;  // 32 warps
+constexpr int RT_WARPS = RT_THREADS / 32;
+constexpr int RT_BATCH = 4;       // 16-byte vector pairs in flight per lane (64-register budget)
 
 __device__ __forceinline__ float dot_bf16x8(uint4 h, uint4 w, float acc) {
   const __nv_bfloat162* hp = reinterpret_cast<const __nv_bfloat162*>(&h);
@@ -42,7 +43,7 @@ __device__ __forceinline__ float dot_bf16x8(uint4 h, uint4 w, float acc) {
 
 __global__ void __launch_bounds__(RT_THREADS) restricted_kernel(const RestrictedArgs a) {
   __shared__ float sZ[JET_MAX_UNION];
-  __shared__ float sRed[2 * (RT_THREADS / 32)];
+  __shared__ float sRed[2 * RT_WARPS];
   pdl_trigger();
   pdl_wait();
   if (*(volatile const int*)a.err != 0) return;
@@ -53,31 +54,23 @@ __global__ void __launch_bounds__(RT_THREADS) restricted_kernel(const Restricted
   const uint4* h = reinterpret_cast<const uint4*>(a.H) + (size_t)r * nvec;
   const uint4* Wv = reinterpret_cast<const uint4*>(a.W);
 
-  for (int g0 = warp * RT_GROUP; g0 < U; g0 += RT_GROUP * (RT_THREADS / 32)) {
-    const int ng = min(RT_GROUP, U - g0);
-    const uint4* w[RT_GROUP];
+  for (int u = warp; u < U; u += RT_WARPS) {
+    const uint4* w = Wv + (size_t)a.union_ids[u] * nvec;
+    float acc = 0.f;
+    for (int k0 = lane; k0 < nvec; k0 += 32 * RT_BATCH) {
+      uint4 hv[RT_BATCH], wv[RT_BATCH];
 #pragma unroll
-    for (int i = 0; i < RT_GROUP; ++i)
-      w[i] = Wv + (size_t)a.union_ids[g0 + min(i, ng - 1)] * nvec;
-    float acc[RT_GROUP];
+      for (int i = 0; i < RT_BATCH; ++i) {
+        const int k = k0 + 32 * i;
+        if (k < nvec) { hv[i] = h[k]; wv[i] = w[k]; }
+      }
 #pragma unroll
-    for (int i = 0; i < RT_GROUP; ++i) acc[i] = 0.f;
-    for (int k = lane; k < nvec; k += 32) {
-      const uint4 hv = h[k];
-#pragma unroll
-      for (int i = 0; i < RT_GROUP; ++i) acc[i] = dot_bf16x8(hv, w[i][k], acc[i]);
+      for (int i = 0; i < RT_BATCH; ++i)
+        if (k0 + 32 * i < nvec) acc = dot_bf16x8(hv[i], wv[i], acc);
     }
 #pragma unroll
-    for (int i = 0; i < RT_GROUP; ++i) {
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], o);
-    }
-    if (lane < ng) {
-      float v = acc[0];
-#pragma unroll
-      for (int i = 1; i < RT_GROUP; ++i) v = (lane == i) ? acc[i] : v;
-      sZ[g0 + lane] = v;
-    }
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) sZ[u] = acc;
   }
   __syncthreads();
 
@@ -90,16 +83,16 @@ __global__ void __launch_bounds__(RT_THREADS) restricted_kernel(const Restricted
   __syncthreads();
   M = sRed[0];
 #pragma unroll
-  for (int i = 1; i < RT_THREADS / 32; ++i) M = fmaxf(M, sRed[i]);
+  for (int i = 1; i < RT_WARPS; ++i) M = fmaxf(M, sRed[i]);
   float sum = 0.f;
   for (int u = threadIdx.x; u < U; u += RT_THREADS) sum += expf(sZ[u] - M);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-  if (lane == 0) sRed[RT_THREADS / 32 + warp] = sum;
+  if (lane == 0) sRed[RT_WARPS + warp] = sum;
   __syncthreads();
   sum = 0.f;
 #pragma unroll
-  for (int i = 0; i < RT_THREADS / 32; ++i) sum += sRed[RT_THREADS / 32 + i];
+  for (int i = 0; i < RT_WARPS; ++i) sum += sRed[RT_WARPS + i];
   const float lse = M + logf(sum);
   if (threadIdx.x == 0 && a.lse) a.lse[r] = lse;
   for (int e = a.row_ptr[r] + threadIdx.x; e < a.row_ptr[r + 1]; e += RT_THREADS) {

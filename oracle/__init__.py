@@ -27,8 +27,7 @@ def build(force: bool = False) -> str:
     """Compile the oracle (gcc, -O2, OpenMP, no fast-math, no FMA contraction)."""
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + f".tmp{os.getpid()}"
-        subprocess.check_call(["gcc", "-std=c11", "-O2", "-fopenmp", "-fPIC", "-ffp-contract=off",
-                               "-Wall", "-shared", "-o", tmp, _SRC, "-lm"])
+        compile_library(_SRC, tmp)
         os.replace(tmp, _LIB)
     return _LIB
 
@@ -36,21 +35,32 @@ def build(force: bool = False) -> str:
 _lib = None
 
 
+def configure(lib: C.CDLL) -> C.CDLL:
+    """Declare the C signatures on a loaded oracle library."""
+    P = C.c_void_p
+    i64 = C.c_int64
+    lib.orc_log_softmax_at.argtypes = [P, i64, i64, P]
+    lib.orc_logits.argtypes = [P, P, i64, i64, i64, P, i64, P]
+    lib.orc_score_tokens.argtypes = [P, P, i64, i64, i64, P, P, i64, P, P, P, C.c_int]
+    lib.orc_score_tokens_restricted.argtypes = [P, P, i64, i64, i64, P, i64, P, P, i64, P, P, P, C.c_int]
+    lib.orc_set_rules.argtypes = [P, P, i64, P, i64, P, P, i64, C.c_double] + [P] * 8
+    lib.orc_score_sets.argtypes = ([P, P, i64, i64, i64, P, P, i64, P, i64, P, P, i64,
+                                    C.c_double, C.c_int, P, i64] + [P] * 10 + [C.c_int])
+    lib.orc_max_threads.argtypes = []
+    return lib
+
+
+def compile_library(src: str, out: str) -> str:
+    """Compile an oracle source file (used by the build and by mutation tests)."""
+    subprocess.check_call(["gcc", "-std=c11", "-O2", "-fopenmp", "-fPIC", "-ffp-contract=off",
+                           "-Wall", "-shared", "-o", out, src, "-lm"])
+    return out
+
+
 def _load():
     global _lib
     if _lib is None:
-        lib = C.CDLL(build())
-        P = C.c_void_p
-        i64 = C.c_int64
-        lib.orc_log_softmax_at.argtypes = [P, i64, i64, P]
-        lib.orc_logits.argtypes = [P, P, i64, i64, i64, P, i64, P]
-        lib.orc_score_tokens.argtypes = [P, P, i64, i64, i64, P, P, i64, P, P, P, C.c_int]
-        lib.orc_score_tokens_restricted.argtypes = [P, P, i64, i64, i64, P, i64, P, P, i64, P, P, P, C.c_int]
-        lib.orc_set_rules.argtypes = [P, P, i64, P, i64, P, P, i64, C.c_double] + [P] * 8
-        lib.orc_score_sets.argtypes = ([P, P, i64, i64, i64, P, P, i64, P, i64, P, P, i64,
-                                        C.c_double, C.c_int, P, i64] + [P] * 10 + [C.c_int])
-        lib.orc_max_threads.argtypes = []
-        _lib = lib
+        _lib = configure(C.CDLL(build()))
     return _lib
 
 
