@@ -147,9 +147,10 @@ def make_workload(name, rank=0):
     return wl, steps
 
 
-def roofline_terms(wl, peaks, sustained):
-    """Algorithmic work of one full-vocabulary head launch and the roofline time."""
-    N, d, V, n_tok = wl.N, wl.d, wl.V, wl.n_tok
+def roofline_terms(wl, peaks, sustained, n_rows=None):
+    """Algorithmic work of one full-vocabulary head launch over n_rows hidden
+    rows (default: all of the workload's rows) and the roofline time."""
+    N, d, V, n_tok = (wl.N if n_rows is None else n_rows), wl.d, wl.V, wl.n_tok
     flops = 2.0 * N * d * V
     bytes_ = 2.0 * V * d + 2.0 * N * d + 8.0 * n_tok
     tc = (peaks["bf16_sustained"] if sustained else peaks["bf16"]) * 1e12
@@ -269,10 +270,19 @@ def gpu_arm(args, world, rank, local):
     sc = jet.JetScorer(wl.d, wl.V, wl.N, wl.n_tok, device=local)
     outs = [sc.alloc_outputs(s.N, s.n_tok, s.n_cand, s.n_sets) for s in steps_wl]
     stream = torch.cuda.Stream(dev)
+    n_rows_scored = wl.N
+    if args.dedup:
+        # candidate-preserving readout: score each distinct hidden row once
+        Hu_buf = [torch.empty_like(x["H"]) for x in ins]
+        with torch.cuda.stream(stream):
+            n_rows_scored = int(sc.dedup_rows(ins[0]["H"], ins[0]["tok_row"], H_unique=Hu_buf[0])[0].shape[0])
 
     def step():
-        for x, o in zip(ins, outs):
-            sc.score_sets(x["H"], Wd, x["tok_row"], x["tok_ids"], x["cand_offsets"], x["set_offsets"], x["kind"],
+        for i, (x, o) in enumerate(zip(ins, outs)):
+            H, tok_row = x["H"], x["tok_row"]
+            if args.dedup:
+                H, tok_row, _ = sc.dedup_rows(H, tok_row, H_unique=Hu_buf[i])
+            sc.score_sets(H, Wd, tok_row, x["tok_ids"], x["cand_offsets"], x["set_offsets"], x["kind"],
                           x["T"], x["mode"], x["union_ids"], out=o, sync=False)
 
     with torch.cuda.stream(stream):
@@ -333,8 +343,8 @@ def gpu_arm(args, world, rank, local):
     # kernel roofline: the full-vocabulary head
     head = prof["head"]
     head_ms = head["ms"] / max(1, head["launches"])
-    flops, bytes_, t_tc, t_hbm = roofline_terms(wl, peaks, sustained=True)
-    _, _, t_tc_burst, _ = roofline_terms(wl, peaks, sustained=False)
+    flops, bytes_, t_tc, t_hbm = roofline_terms(wl, peaks, sustained=True, n_rows=n_rows_scored)
+    _, _, t_tc_burst, _ = roofline_terms(wl, peaks, sustained=False, n_rows=n_rows_scored)
     # bound by the roofline formula with the burst tensor peak; the tensor
     # denominator is the sustained peak, since the head runs inside a long loop
     bound = "hbm" if t_hbm >= t_tc_burst else "tensor"
@@ -357,7 +367,8 @@ def gpu_arm(args, world, rank, local):
             "parallelism": f"replicas x{world}",
             "l2": "inputs larger than L2 (W = %.2f GB > 129 MB L2)" % (wl.W.nbytes / 1e9),
             "accumulate": "fp32 (tcgen05 bf16 x bf16 -> fp32 TMEM)",
-            "plan": sc.plan_info(wl.N),
+            "plan": sc.plan_info(n_rows_scored),
+            "row_dedup": bool(args.dedup), "rows_scored": n_rows_scored,
             "step_roofline_us": t_roof * 1e6, "step_roofline_frac": t_roof / (ms_step / 1e3),
             "kernel_ms_per_step": {k: v["ms"] / K for k, v in prof.items() if isinstance(v, dict)},
             "ms_per_step_with_kernel_events": ms_prof / K,
@@ -443,6 +454,8 @@ def main():
     ap.add_argument("--workload", default="binary", choices=sorted(WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--dedup", action="store_true",
+                    help="score each distinct hidden row once (jet_dedup_rows before every step)")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     if args.impl == "reference":

@@ -5,6 +5,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <algorithm>
 #include <new>
 #include <vector>
 
@@ -112,6 +113,10 @@ struct jet_ctx {
   int32_t *st_row = nullptr, *st_tok = nullptr, *st_co = nullptr, *st_so = nullptr, *st_union = nullptr;
   uint8_t* st_kind = nullptr;
   int* h_err = nullptr;   // pinned
+  // row deduplication workspace
+  unsigned long long *dd_hash = nullptr, *dd_keys = nullptr;
+  int *dd_vals = nullptr, *dd_rep = nullptr, *dd_rank = nullptr;
+  int dd_table = 0;
   // schedule cache
   int plan_rows = -1;
   Plan plan;
@@ -409,7 +414,14 @@ int jet_create(jet_ctx** out, int d, int V, int max_rows, int max_tokens, int de
   A(dalloc(&c->st_so, Tk + 1));
   A(dalloc(&c->st_kind, Tk));
   A(dalloc(&c->st_union, (size_t)JET_MAX_UNION));
-  A(cudaMallocHost(reinterpret_cast<void**>(&c->h_err), ERR_WORDS * sizeof(int)));
+  c->dd_table = 1;
+  while (c->dd_table < 2 * max_rows) c->dd_table <<= 1;
+  A(dalloc(&c->dd_hash, R));
+  A(dalloc(&c->dd_keys, (size_t)c->dd_table));
+  A(dalloc(&c->dd_vals, (size_t)c->dd_table));
+  A(dalloc(&c->dd_rep, R));
+  A(dalloc(&c->dd_rank, R + 1));
+  A(cudaMallocHost(reinterpret_cast<void**>(&c->h_err), 2 * ERR_WORDS * sizeof(int)));   // + result words
   A(cudaMemset(c->err, 0, ERR_WORDS * sizeof(int)));
   if (e != cudaSuccess) {
     jet_destroy(c);
@@ -425,13 +437,56 @@ void jet_destroy(jet_ctx* c) {
   cudaDeviceSynchronize();
   void* ptrs[] = {c->err, c->row_ptr, c->row_cur, c->row_list, c->upos, c->zg, c->part, c->hash,
                   c->lse, c->logp, c->s, c->q, c->qe, c->dec, c->expd, c->conf, c->mass, c->stH,
-                  c->st_row, c->st_tok, c->st_co, c->st_so, c->st_kind, c->st_union};
+                  c->st_row, c->st_tok, c->st_co, c->st_so, c->st_kind, c->st_union,
+                  c->dd_hash, c->dd_keys, c->dd_vals, c->dd_rep, c->dd_rank};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   for (auto& v : c->ev)
     for (cudaEvent_t e : v) cudaEventDestroy(e);
   if (c->h_err) cudaFreeHost(c->h_err);
   delete c;
+}
+
+int jet_dedup_rows(jet_ctx* c, const void* H, int n_rows, const int32_t* tok_row, int n_tok, void* H_unique,
+                   int32_t* tok_row_unique, int32_t* row_map, int* n_unique, void* stream) {
+  if (!c || !n_unique || n_rows < 1 || n_tok < 0) return JET_ERR_ARG;
+  if (n_rows > c->max_rows || n_tok > c->max_tokens) return JET_ERR_WORKSPACE;
+  if (!H || !H_unique || (n_tok > 0 && (!tok_row || !tok_row_unique))) return JET_ERR_ARG;
+  if (!aligned16(H) || !aligned16(H_unique)) return JET_ERR_ARG;
+  const size_t bytes = (size_t)n_rows * c->d * 2;
+  const uintptr_t h0 = reinterpret_cast<uintptr_t>(H), u0 = reinterpret_cast<uintptr_t>(H_unique);
+  if (h0 < u0 + bytes && u0 < h0 + bytes) return JET_ERR_ARG;   // must not overlap
+  DeviceGuard g(c->device);
+  if (!g.ok) return JET_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int table = 1;
+  while (table < 2 * n_rows) table <<= 1;
+  DedupArgs a;
+  a.n_rows = n_rows;
+  a.d = c->d;
+  a.n_tok = n_tok;
+  a.H = static_cast<const uint16_t*>(H);
+  a.tok_row = tok_row;
+  a.H_unique = static_cast<uint16_t*>(H_unique);
+  a.tok_row_unique = tok_row_unique;
+  a.row_map = row_map;
+  a.hash = c->dd_hash;
+  a.keys = c->dd_keys;
+  a.vals = c->dd_vals;
+  a.table = table;
+  a.rep = c->dd_rep;
+  a.rank = c->dd_rank;
+  a.err = c->err;
+  if (launch_dedup(a, st) != cudaSuccess) {
+    cudaStreamSynchronize(st);
+    return JET_ERR_CUDA;
+  }
+  int* h_count = c->h_err + ERR_WORDS;   // pinned word after the error block
+  if (cudaMemcpyAsync(h_count, c->dd_rank + n_rows, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return JET_ERR_CUDA;
+  const int rc = read_status(c, st);
+  if (rc == JET_OK) *n_unique = *h_count;
+  return rc;
 }
 
 int jet_profile_enable(jet_ctx* c, int enable) {

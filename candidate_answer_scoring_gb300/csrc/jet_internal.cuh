@@ -185,6 +185,20 @@ struct SetArgs {
 };
 cudaError_t launch_sets(const SetArgs& a, cudaStream_t st);
 
+struct DedupArgs {
+  int n_rows, d, n_tok;
+  const uint16_t* H; const int32_t* tok_row;
+  uint16_t* H_unique; int32_t* tok_row_unique; int32_t* row_map;   // row_map may be NULL
+  unsigned long long* hash;   // [n_rows]
+  unsigned long long* keys;   // [table]
+  int* vals;                  // [table]
+  int table;                  // power of two >= 2 * n_rows
+  int* rep;                   // [n_rows]
+  int* rank;                  // [n_rows + 1]; rank[n_rows] = distinct rows
+  int* err;
+};
+cudaError_t launch_dedup(const DedupArgs& a, cudaStream_t st);
+
 // One CTA waits on an mbarrier that nothing completes, with a limit of
 // limit_ns; the bounded wait records JET_ERR_TIMEOUT (where = 99) in err.
 cudaError_t launch_wait_selftest(int* err, unsigned long long limit_ns, cudaStream_t st);

@@ -75,6 +75,7 @@ def load() -> C.CDLL:
     lib.jet_profile_enable.argtypes = [P, I]
     lib.jet_profile_read.argtypes = [P, C.POINTER(C.c_double), I]
     lib.jet_selftest_wait_timeout.argtypes = [P, I, P]
+    lib.jet_dedup_rows.argtypes = [P, P, I, P, I, P, P, P, C.POINTER(C.c_int), P]
     _lib = lib
     return lib
 
@@ -206,6 +207,24 @@ class JetScorer:
         res = {k: {"launches": int(out[2 * i]), "ms": float(out[2 * i + 1])} for i, k in enumerate(self.KERNELS)}
         res["untimed_launches"] = int(out[10])
         return res
+
+    def dedup_rows(self, H: torch.Tensor, tok_row: torch.Tensor, H_unique: Optional[torch.Tensor] = None,
+                   want_row_map: bool = False):
+        """Distinct rows of H (first occurrences, in order) and the tokens' rows
+        in them: returns (H_unique[:n_unique], tok_row_unique, row_map or None)."""
+        dev = self.device
+        _check_dev(H, "H", dev, _BF16)
+        _check_dev(tok_row, "tok_row", dev, (torch.int32,))
+        if H_unique is None:
+            H_unique = torch.empty_like(H)
+        tok_u = torch.empty_like(tok_row)
+        row_map = torch.empty(H.shape[0], dtype=torch.int32, device=dev) if want_row_map else None
+        n = C.c_int(0)
+        rc = self.lib.jet_dedup_rows(self._h, _ptr(H), H.shape[0], _ptr(tok_row), tok_row.numel(), _ptr(H_unique),
+                                     _ptr(tok_u), _ptr(row_map), C.byref(n), _stream(dev))
+        if rc != JET_OK:
+            raise JetError(rc, "jet_dedup_rows")
+        return H_unique[:n.value], tok_u, row_map
 
     def selftest_wait_timeout(self, limit_us: int) -> int:
         """Run the bounded-wait diagnostic; returns the status (JET_ERR_TIMEOUT expected)."""

@@ -177,6 +177,30 @@ int jet_score_sets_host(jet_ctx *ctx, const void *H_bf16_host, const void *W_bf1
                         void *cuda_stream);
 
 /*
+ * jet_dedup_rows: project each distinct predictor state once -- the
+ * candidate-preserving readout of FastJEV (section 3.3: project each required
+ * predictor node once, normalise over the full vocabulary, gather the token
+ * log-probabilities along each candidate path).  Finds bitwise-identical rows
+ * of H (candidates sharing a token history carry identical hidden states) and
+ * writes the distinct rows, in order of first occurrence, to H_unique; each
+ * token's row is remapped so that scoring (H_unique, tok_row_unique) gives the
+ * same results as scoring (H, tok_row).  Rows are compared by content (a
+ * 64-bit hash, confirmed byte by byte), so different rows are never merged.
+ *   H [n_rows, d] bf16 (device, 16-byte aligned); tok_row [n_tok] int32.
+ *   H_unique [n_rows, d] bf16 (device, caller-owned, must not overlap H):
+ *     rows 0 .. *n_unique-1 are written.
+ *   tok_row_unique [n_tok] int32 (device): row of each token in H_unique.
+ *   row_map [n_rows] int32 (device) or NULL: H_unique row of each input row.
+ *   *n_unique (host): number of distinct rows.
+ * Errors: JET_ERR_ARG (pointers, alignment, overlap, sizes), JET_ERR_WORKSPACE
+ * (beyond jet_create's sizes), JET_ERR_TOKEN_RANGE (a tok_row outside
+ * [0, n_rows)), JET_ERR_CUDA.  Synchronous.
+ */
+int jet_dedup_rows(jet_ctx *ctx, const void *H_bf16, int n_rows, const int32_t *tok_row, int n_tok,
+                   void *H_unique_bf16, int32_t *tok_row_unique, int32_t *row_map, int *n_unique,
+                   void *cuda_stream);
+
+/*
  * jet_plan_info: the vocabulary-split schedule the full-vocabulary head uses
  * for `n_rows` rows (for reports and tests).  info[0..7] receive:
  *   row tiles, vocabulary tiles, splits per row tile, band height (row tiles
