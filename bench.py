@@ -445,6 +445,87 @@ def gpu_arm(args, world, rank, local):
     return 0
 
 
+# ---------------------------------------------------------------------------
+# the widened rows: row dedup, temperature fitting, layer sensitivity
+# ---------------------------------------------------------------------------
+def time_op(fn, K, W):
+    import torch
+    for _ in range(W):
+        fn()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(K):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / K
+
+
+def op_arm(args):
+    """One JSON line for a widened op (not the headline scoring metric)."""
+    import numpy as np
+    import torch
+
+    import candidate_answer_scoring_gb300 as jet
+    import workloads as wk
+    from candidate_answer_scoring_gb300 import build as libbuild
+    libbuild.build()
+    peaks = load_peaks()
+    dev = torch.device("cuda", 0)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    K = args.steps if args.steps is not None else 50
+    W = max(3, args.warmup if args.warmup is not None else 5)
+    line = {"op": args.op, "n_gpus": 1, "steps": K, "warmup": W, "data": "synthetic"}
+    if args.op == "dedup":
+        wl = wk.large_choice()
+        sc = jet.JetScorer(wl.d, wl.V, wl.N, wl.n_tok)
+        H = t(wl.H.view(np.int16)).view(torch.bfloat16)
+        tok_row = t(wl.tok_row)
+        Hu = torch.empty_like(H)
+        n_u = sc.dedup_rows(H, tok_row, H_unique=Hu)[0].shape[0]
+        ms = time_op(lambda: sc.dedup_rows(H, tok_row, H_unique=Hu), K, W)
+        nbytes = 2.0 * wl.N * wl.d + 2.0 * 2 * n_u * wl.d + 8.0 * wl.n_tok   # hash read, copy read+write
+        line.update(metric="hidden rows deduplicated per second", value=wl.N / (ms / 1e3), unit="rows/s",
+                    ms=ms, config={"workload": "large choice H: %d rows x d=%d, %d distinct" % (wl.N, wl.d, n_u)},
+                    roofline={"bound": "hbm", "achieved": nbytes / (ms / 1e3) / 1e9, "peak": peaks["hbm"],
+                              "unit": "GB/s", "frac": nbytes / (ms / 1e3) / 1e9 / peaks["hbm"],
+                              "note": "synchronous call: includes the count read-back"})
+    elif args.op == "fit_temperature":
+        wl = wk.wide_schema()
+        import oracle
+        r = oracle.score_workload(wk.wide_schema(n_requests=2))     # scores of 64 fields, tiled to 512
+        rng = np.random.default_rng(0)
+        s = np.resize(r.s.astype(np.float32), wl.n_cand)
+        gold = np.array([rng.integers(0, wl.set_offsets[k + 1] - wl.set_offsets[k]) for k in range(wl.n_sets)],
+                        np.int32)
+        sc = jet.JetScorer(64, 100, 4, wl.n_tok)
+        args_ = [t(s), t(wl.tok_ids), t(wl.cand_offsets), t(wl.set_offsets), t(gold)]
+        T, nll = sc.fit_temperature(*args_)
+        ms = time_op(lambda: sc.fit_temperature(*args_), K, W)
+        line.update(metric="temperature fits per second", value=1e3 / ms, unit="fits/s", ms=ms, T=T, nll=nll,
+                    config={"workload": "wide schema: %d sets, %d candidates" % (wl.n_sets, wl.n_cand)},
+                    roofline={"bound": "latency", "note": "one CTA, bracketed Newton on 1/T; synchronous call"})
+    elif args.op == "layer_sensitivity":
+        rng = np.random.default_rng(0)
+        n, L, m = 4096, 64, 64
+        offsets = np.arange(0, n * m + 1, m, dtype=np.int32)
+        z = rng.normal(-20, 6, size=n * m).astype(np.float32)
+        z_skip = (z[None, :] + rng.normal(size=(L, n * m)) * 0.1).astype(np.float32)
+        sc = jet.JetScorer(64, 100, 4, 4)
+        a = [t(z), t(z_skip), t(offsets)]
+        ms = time_op(lambda: sc.layer_sensitivity(*a, 8), K, W)
+        nbytes = 4.0 * (L + 1) * n * m + 4.0 * L * n
+        line.update(metric="layer-input sensitivities per second", value=L * n / (ms / 1e3), unit="1/s", ms=ms,
+                    config={"workload": "%d inputs x %d logits x %d layers" % (n, m, L)},
+                    roofline={"bound": "hbm", "achieved": nbytes / (ms / 1e3) / 1e9, "peak": peaks["hbm"],
+                              "unit": "GB/s", "frac": nbytes / (ms / 1e3) / 1e9 / peaks["hbm"],
+                              "note": "synchronous call: includes the status read-back"})
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -456,8 +537,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--dedup", action="store_true",
                     help="score each distinct hidden row once (jet_dedup_rows before every step)")
+    ap.add_argument("--op", default=None, choices=["dedup", "fit_temperature", "layer_sensitivity"],
+                    help="time one of the widened ops instead of the scoring path")
     args = ap.parse_args()
     world, rank, local = dist_setup()
+    if args.op is not None:
+        return op_arm(args)
     if args.impl == "reference":
         return reference_arm(args, world, rank)
     return gpu_arm(args, world, rank, local)

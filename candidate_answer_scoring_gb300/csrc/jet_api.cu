@@ -117,6 +117,8 @@ struct jet_ctx {
   unsigned long long *dd_hash = nullptr, *dd_keys = nullptr;
   int *dd_vals = nullptr, *dd_rep = nullptr, *dd_rank = nullptr;
   int dd_table = 0;
+  // temperature fitting
+  double *fit_res = nullptr, *h_fit = nullptr;   // device [3], pinned host [3]
   // schedule cache
   int plan_rows = -1;
   Plan plan;
@@ -421,6 +423,8 @@ int jet_create(jet_ctx** out, int d, int V, int max_rows, int max_tokens, int de
   A(dalloc(&c->dd_vals, (size_t)c->dd_table));
   A(dalloc(&c->dd_rep, R));
   A(dalloc(&c->dd_rank, R + 1));
+  A(dalloc(&c->fit_res, 3));
+  A(cudaMallocHost(reinterpret_cast<void**>(&c->h_fit), 3 * sizeof(double)));
   A(cudaMallocHost(reinterpret_cast<void**>(&c->h_err), 2 * ERR_WORDS * sizeof(int)));   // + result words
   A(cudaMemset(c->err, 0, ERR_WORDS * sizeof(int)));
   if (e != cudaSuccess) {
@@ -444,6 +448,8 @@ void jet_destroy(jet_ctx* c) {
   for (auto& v : c->ev)
     for (cudaEvent_t e : v) cudaEventDestroy(e);
   if (c->h_err) cudaFreeHost(c->h_err);
+  if (c->h_fit) cudaFreeHost(c->h_fit);
+  if (c->fit_res) cudaFree(c->fit_res);
   delete c;
 }
 
@@ -487,6 +493,71 @@ int jet_dedup_rows(jet_ctx* c, const void* H, int n_rows, const int32_t* tok_row
   const int rc = read_status(c, st);
   if (rc == JET_OK) *n_unique = *h_count;
   return rc;
+}
+
+int jet_fit_temperature(jet_ctx* c, const float* s, const int32_t* tok_ids, int n_tok, const int32_t* cand_offsets,
+                        int n_cand, const int32_t* set_offsets, int n_sets, const int32_t* gold, double T_min,
+                        double T_max, double* T_out, double* nll_out, void* stream) {
+  if (!c || !s || !tok_ids || !cand_offsets || !set_offsets || !gold || !T_out) return JET_ERR_ARG;
+  if (n_sets < 1 || n_cand < n_sets || n_tok < n_cand) return JET_ERR_OFFSETS;
+  if (n_tok > c->max_tokens) return JET_ERR_WORKSPACE;
+  if (!(T_min > 0.0) || !(T_max > T_min) || !std::isfinite(T_max)) return JET_ERR_ARG;
+  DeviceGuard g(c->device);
+  if (!g.ok) return JET_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  FitArgs a;
+  a.n_sets = n_sets;
+  a.n_cand = n_cand;
+  a.n_tok = n_tok;
+  a.s = s;
+  a.tok_ids = tok_ids;
+  a.cand_offsets = cand_offsets;
+  a.set_offsets = set_offsets;
+  a.gold = gold;
+  a.T_min = T_min;
+  a.T_max = T_max;
+  a.flags = reinterpret_cast<uint8_t*>(c->upos);   // [max_tokens] ints of scratch, n_cand bytes used
+  a.result = c->fit_res;
+  a.err = c->err;
+  if (launch_fit_temperature(a, st) != cudaSuccess) {
+    cudaStreamSynchronize(st);
+    return JET_ERR_CUDA;
+  }
+  if (cudaMemcpyAsync(c->h_fit, c->fit_res, 3 * sizeof(double), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return JET_ERR_CUDA;
+  const int rc = read_status(c, st);
+  if (rc == JET_OK) {
+    *T_out = c->h_fit[0];
+    if (nll_out) *nll_out = c->h_fit[1];
+  }
+  return rc;
+}
+
+int jet_layer_sensitivity(jet_ctx* c, const float* z, const float* z_skip, const int32_t* offsets, int n_inputs,
+                          int total, int L, int k, float* d, float* J, int32_t* selected, void* stream) {
+  if (!c || !z || !z_skip || !offsets || !d || !J || n_inputs < 1 || total < n_inputs || L < 1 || k < 0 || k > L)
+    return JET_ERR_ARG;
+  if (k > 0 && !selected) return JET_ERR_ARG;
+  DeviceGuard g(c->device);
+  if (!g.ok) return JET_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  SensArgs a;
+  a.n_inputs = n_inputs;
+  a.L = L;
+  a.total = total;
+  a.k = k;
+  a.z = z;
+  a.z_skip = z_skip;
+  a.offsets = offsets;
+  a.d = d;
+  a.J = J;
+  a.selected = selected;
+  a.err = c->err;
+  if (launch_sensitivity(a, st) != cudaSuccess) {
+    cudaStreamSynchronize(st);
+    return JET_ERR_CUDA;
+  }
+  return read_status(c, st);
 }
 
 int jet_profile_enable(jet_ctx* c, int enable) {

@@ -199,6 +199,29 @@ struct DedupArgs {
 };
 cudaError_t launch_dedup(const DedupArgs& a, cudaStream_t st);
 
+struct FitArgs {
+  int n_sets, n_cand, n_tok;
+  const float* s; const int32_t* tok_ids; const int32_t* cand_offsets; const int32_t* set_offsets;
+  const int32_t* gold;        // [n_sets] index within the set of the gold candidate
+  double T_min, T_max;
+  uint8_t* flags;             // [n_cand] scratch: member of its set's gold class
+  double* result;             // [3]: T, mean NLL at T, iterations
+  int* err;
+};
+cudaError_t launch_fit_temperature(const FitArgs& a, cudaStream_t st);
+
+struct SensArgs {
+  int n_inputs, L, total, k;
+  const float* z;             // [total] logits of every input, CSR by offsets
+  const float* z_skip;        // [L][total] the same with layer l skipped
+  const int32_t* offsets;     // [n_inputs + 1]
+  float* d;                   // [L][n_inputs]
+  float* J;                   // [L]
+  int32_t* selected;          // [k]
+  int* err;
+};
+cudaError_t launch_sensitivity(const SensArgs& a, cudaStream_t st);
+
 // One CTA waits on an mbarrier that nothing completes, with a limit of
 // limit_ns; the bounded wait records JET_ERR_TIMEOUT (where = 99) in err.
 cudaError_t launch_wait_selftest(int* err, unsigned long long limit_ns, cudaStream_t st);

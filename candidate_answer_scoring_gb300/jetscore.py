@@ -76,6 +76,9 @@ def load() -> C.CDLL:
     lib.jet_profile_read.argtypes = [P, C.POINTER(C.c_double), I]
     lib.jet_selftest_wait_timeout.argtypes = [P, I, P]
     lib.jet_dedup_rows.argtypes = [P, P, I, P, I, P, P, P, C.POINTER(C.c_int), P]
+    lib.jet_layer_sensitivity.argtypes = [P, P, P, P, I, I, I, I, P, P, P, P]
+    lib.jet_fit_temperature.argtypes = [P, P, P, I, P, I, P, I, P, C.c_double, C.c_double,
+                                        C.POINTER(C.c_double), C.POINTER(C.c_double), P]
     _lib = lib
     return lib
 
@@ -225,6 +228,39 @@ class JetScorer:
         if rc != JET_OK:
             raise JetError(rc, "jet_dedup_rows")
         return H_unique[:n.value], tok_u, row_map
+
+    def fit_temperature(self, s, tok_ids, cand_offsets, set_offsets, gold, T_min: float = 0.05,
+                        T_max: float = 100.0):
+        """Temperature minimising the mean gold NLL; returns (T, nll)."""
+        dev = self.device
+        _check_dev(s, "s", dev, (torch.float32,))
+        for name, t in (("tok_ids", tok_ids), ("cand_offsets", cand_offsets), ("set_offsets", set_offsets),
+                        ("gold", gold)):
+            _check_dev(t, name, dev, (torch.int32,))
+        T, nll = C.c_double(0), C.c_double(0)
+        rc = self.lib.jet_fit_temperature(self._h, _ptr(s), _ptr(tok_ids), tok_ids.numel(), _ptr(cand_offsets),
+                                          cand_offsets.numel() - 1, _ptr(set_offsets), set_offsets.numel() - 1,
+                                          _ptr(gold), float(T_min), float(T_max), C.byref(T), C.byref(nll),
+                                          _stream(dev))
+        if rc != JET_OK:
+            raise JetError(rc, "jet_fit_temperature")
+        return T.value, nll.value
+
+    def layer_sensitivity(self, z, z_skip, offsets, k: int):
+        """(d [L, n], J [L], selected [k]) of the layer-sensitivity ranking."""
+        dev = self.device
+        _check_dev(z, "z", dev, (torch.float32,))
+        _check_dev(z_skip, "z_skip", dev, (torch.float32,))
+        _check_dev(offsets, "offsets", dev, (torch.int32,))
+        L, n = z_skip.shape[0], offsets.numel() - 1
+        d = torch.empty((L, n), dtype=torch.float32, device=dev)
+        J = torch.empty(L, dtype=torch.float32, device=dev)
+        sel = torch.empty(max(k, 1), dtype=torch.int32, device=dev)
+        rc = self.lib.jet_layer_sensitivity(self._h, _ptr(z), _ptr(z_skip), _ptr(offsets), n, z.numel(), L, int(k),
+                                            _ptr(d), _ptr(J), _ptr(sel), _stream(dev))
+        if rc != JET_OK:
+            raise JetError(rc, "jet_layer_sensitivity")
+        return d, J, sel[:k]
 
     def selftest_wait_timeout(self, limit_us: int) -> int:
         """Run the bounded-wait diagnostic; returns the status (JET_ERR_TIMEOUT expected)."""

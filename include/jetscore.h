@@ -201,6 +201,50 @@ int jet_dedup_rows(jet_ctx *ctx, const void *H_bf16, int n_rows, const int32_t *
                    void *cuda_stream);
 
 /*
+ * jet_fit_temperature: fit the set-softmax temperature to labelled sets (the
+ * calibration step of the Gemma/MLX architecture page, "Output contracts") by
+ * minimising the mean gold negative log-likelihood
+ *   NLL(T) = mean_k -log sum_{c in G_k} q_c(T),   q = softmax over the set of s/T,
+ * where G_k holds the candidates of set k with the gold candidate's token
+ * sequence (gold probability summed over labels with identical text, JET
+ * Eq. 5 discussion).  NLL is convex in 1/T; the fit is a bracketed Newton
+ * iteration on 1/T over [T_min, T_max] in one CTA.
+ *   s [n_cand] fp32 (device): sequence log-likelihoods, e.g. jet_score_sets' s
+ *   tok_ids [n_tok], cand_offsets [n_cand+1], set_offsets [n_sets+1]: as in
+ *     jet_score_sets (device)
+ *   gold [n_sets] int32 (device): index within each set of the gold candidate
+ *   0 < T_min < T_max (finite)
+ *   *T_out (host): fitted temperature (T_min or T_max when the optimum lies
+ *     at the boundary); *nll_out (host) or NULL: mean NLL at *T_out
+ * Errors: JET_ERR_ARG, JET_ERR_OFFSETS (offsets or a gold index out of
+ * range), JET_ERR_WORKSPACE (n_tok beyond jet_create's max_tokens),
+ * JET_ERR_CUDA.  Synchronous.
+ */
+int jet_fit_temperature(jet_ctx *ctx, const float *s, const int32_t *tok_ids, int n_tok,
+                        const int32_t *cand_offsets, int n_cand, const int32_t *set_offsets, int n_sets,
+                        const int32_t *gold, double T_min, double T_max, double *T_out, double *nll_out,
+                        void *cuda_stream);
+
+/*
+ * jet_layer_sensitivity: decision-guided layer ranking ("FastJEV: Understanding
+ * Redundancy for Compact JEV Inference", section 3.4, Eq. 5-6):
+ *   d_l(x) = rms(ctr(z^(-l)(x) - z(x))) / max(1e-8, rms(ctr(z(x)))),
+ *   J_l = mean over inputs x of d_l(x),  selected = the k layers with the
+ *   smallest J_l, ties resolved by layer index,
+ * with ctr(v) = v - mean(v) and rms(v) = ||v||_2 / sqrt(len v).
+ *   z [total] fp32 (device): the decision logits of every calibration input,
+ *     input x owning entries offsets[x] .. offsets[x+1]-1 (at least one)
+ *   z_skip [L, total] fp32 (device): the same logits with layer l skipped
+ *   offsets [n_inputs+1] int32 (device), offsets[0] = 0, offsets[n] = total
+ *   d [L, n_inputs], J [L] fp32 (device, caller-owned); selected [k] int32
+ *     (device; may be NULL when k == 0)
+ * Errors: JET_ERR_ARG (sizes, k outside [0, L]), JET_ERR_OFFSETS.  Synchronous.
+ */
+int jet_layer_sensitivity(jet_ctx *ctx, const float *z, const float *z_skip, const int32_t *offsets,
+                          int n_inputs, int total, int L, int k, float *d, float *J, int32_t *selected,
+                          void *cuda_stream);
+
+/*
  * jet_plan_info: the vocabulary-split schedule the full-vocabulary head uses
  * for `n_rows` rows (for reports and tests).  info[0..7] receive:
  *   row tiles, vocabulary tiles, splits per row tile, band height (row tiles

@@ -1,0 +1,64 @@
+"""jet_layer_sensitivity against the fp64 oracle (oracle/sensitivity.py).
+
+Tolerance (fp32 two-pass statistics): d and J within 1e-4 relative; the
+selection exact wherever neighbouring J values differ by more than 1e-4
+relative, and otherwise a valid ordering."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import sensitivity as sens
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def scorer():
+    import candidate_answer_scoring_gb300 as jet
+    return jet.JetScorer(64, 100, 4, 4)
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def case(seed, n=40, L=36, const_input=False):
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(2, 66, size=n)
+    offsets = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    total = int(offsets[-1])
+    z = rng.normal(-20, 6, size=total).astype(np.float32)
+    if const_input:
+        z[offsets[0]:offsets[1]] = -7.0
+    scale = np.exp(rng.normal(-2, 1.5, size=L))           # layers differ in how much they move the logits
+    z_skip = (z[None, :] + scale[:, None] * rng.normal(size=(L, total)) + rng.normal(size=(L, 1)) * 3).astype(np.float32)
+    return z, z_skip, offsets
+
+
+@pytest.mark.parametrize("seed,const_input", [(0, False), (1, False), (2, True)])
+def test_matches_oracle(scorer, seed, const_input):
+    z, z_skip, offsets = case(seed, const_input=const_input)
+    k = 6
+    d, J, sel = scorer.layer_sensitivity(dev(z), dev(z_skip), dev(offsets), k)
+    torch.cuda.synchronize()
+    d_ref, J_ref, sel_ref = sens.layer_sensitivity(z.astype(np.float64), z_skip.astype(np.float64), offsets, k)
+    np.testing.assert_allclose(d.cpu().numpy(), d_ref, rtol=1e-4, atol=0)
+    np.testing.assert_allclose(J.cpu().numpy(), J_ref, rtol=1e-4, atol=0)
+    order = np.argsort(J_ref, kind="stable")
+    gaps = np.diff(J_ref[order]) / np.maximum(J_ref[order][1:], 1e-30)
+    if np.all(gaps[:k] > 1e-4):
+        assert list(sel.cpu().numpy()) == list(sel_ref)
+    else:
+        Jg = J.cpu().numpy()
+        s = sel.cpu().numpy()
+        assert len(set(s)) == k and np.all(np.diff(Jg[s]) >= 0)
+
+
+def test_rejects_empty_input(scorer):
+    import candidate_answer_scoring_gb300 as jet
+    z, z_skip, offsets = case(3, n=5, L=4)
+    bad = offsets.copy()
+    bad[2] = bad[1]
+    with pytest.raises(jet.JetError) as e:
+        scorer.layer_sensitivity(dev(z), dev(z_skip), dev(bad), 2)
+    assert e.value.status == -3
