@@ -84,6 +84,11 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 constexpr int UNITS_PER_SM_CAP = 64;   // bound on schedule units (partials workspace)
+// Restricted path: logits over the union are kept in an [N, |U|] scratch of
+// max(max_rows * 128, 2^20) floats; larger products recompute the scored
+// logits in the set kernel instead.
+constexpr size_t ZU_FLOATS_PER_ROW = 128;
+constexpr size_t ZU_FLOATS_MIN = size_t(1) << 20;
 
 template <class T>
 cudaError_t dalloc(T** p, size_t n) {
@@ -100,7 +105,11 @@ struct jet_ctx {
   int* row_ptr = nullptr;
   int* row_cur = nullptr;
   int2* row_list = nullptr;
-  int* upos = nullptr;
+  int* iscratch = nullptr;   // [max_tokens] ints (temperature fit flags)
+  float* lse_row = nullptr;  // [max_rows] per-row lse handed from merge / restricted head to the set kernel
+  int* umap = nullptr;       // [V] token id -> union position (restricted path)
+  float* zu = nullptr;       // [zu_cap] logits over the union (restricted path)
+  size_t zu_cap = 0;
   float* zg = nullptr;
   float2* part = nullptr;
   unsigned long long* hash = nullptr;
@@ -198,9 +207,11 @@ const Plan& plan_for(jet_ctx* c, int n_rows) {
   return c->plan;
 }
 
-// Full-vocabulary log-probabilities for the rows/tokens the pre-pass listed.
+// Full-vocabulary head and merge for the rows/tokens the pre-pass listed.
+// lse_row NULL: one token per row, logp[r] written by the merge; else the
+// merge leaves each row's lse in lse_row for the set kernel.
 int run_full_head(jet_ctx* c, const void* H, const void* W, int n_rows, float* logp, float* lse,
-                  cudaStream_t st) {
+                  float* lse_row, cudaStream_t st) {
   const Plan& plan = plan_for(c, n_rows);
   CUtensorMap tmH, tmW;
   int rc = encode_kmajor(c, &tmH, H, n_rows, BM);
@@ -229,9 +240,8 @@ int run_full_head(jet_ctx* c, const void* H, const void* W, int n_rows, float* l
   ma.plan = ha.plan;
   ma.part = c->part;
   ma.zg = c->zg;
-  ma.row_ptr = c->row_ptr;
-  ma.row_list = c->row_list;
   ma.lse = lse;
+  ma.lse_row = lse_row;
   ma.logp = logp;
   ma.err = c->err;
   ProfScope ps(c, K_MERGE, st);
@@ -263,58 +273,10 @@ int score_sets_enqueue(jet_ctx* c, const void* H, const void* W, int n_rows, con
   jet_set_out o;
   std::memset(&o, 0, sizeof o);
   if (out) o = *out;
-  float* logp = o.logp ? o.logp : c->logp;
-  float* lse = o.lse;
-
-  PrepArgs pa;
-  pa.n_rows = n_rows;
-  pa.n_tok = n_tok;
-  pa.V = c->V;
-  pa.tok_row = tok_row;
-  pa.tok_ids = tok_ids;
-  pa.cand_offsets = cand_offsets;
-  pa.n_cand = n_cand;
-  pa.set_offsets = set_offsets;
-  pa.kind = kind;
-  pa.n_sets = n_sets;
-  pa.mode = mode;
-  pa.union_ids = union_ids;
-  pa.n_union = mode == JET_MODE_RESTRICTED ? n_union : 0;
-  pa.row_ptr = c->row_ptr;
-  pa.row_cur = c->row_cur;
-  pa.row_list = c->row_list;
-  pa.upos = c->upos;
-  pa.err = c->err;
-  {
-    ProfScope ps(c, K_PREP, st);
-    if (launch_prep(pa, st) != cudaSuccess) return JET_ERR_CUDA;
-  }
-
-  int rc;
-  if (mode == JET_MODE_FULL) {
-    rc = run_full_head(c, H, W, n_rows, logp, lse, st);
-  } else {
-    RestrictedArgs ra;
-    ra.N = n_rows;
-    ra.d = c->d;
-    ra.n_union = n_union;
-    ra.H = static_cast<const uint16_t*>(H);
-    ra.W = static_cast<const uint16_t*>(W);
-    ra.union_ids = union_ids;
-    ra.row_ptr = c->row_ptr;
-    ra.row_list = c->row_list;
-    ra.upos = c->upos;
-    ra.lse = lse;
-    ra.logp = logp;
-    ra.err = c->err;
-    ProfScope ps(c, K_RESTRICTED, st);
-    rc = cuda_status(launch_restricted(ra, st));
-  }
-  if (rc != JET_OK) return rc;
 
   SetArgs sa;
   sa.n_sets = n_sets;
-  sa.logp = logp;
+  sa.logp = o.logp ? o.logp : c->logp;
   sa.tok_ids = tok_ids;
   sa.cand_offsets = cand_offsets;
   sa.set_offsets = set_offsets;
@@ -327,7 +289,65 @@ int score_sets_enqueue(jet_ctx* c, const void* H, const void* W, int n_rows, con
   sa.confidence = o.confidence ? o.confidence : c->conf;
   sa.mass = o.mass ? o.mass : c->mass;
   sa.hash = c->hash;
+  sa.zg = nullptr;
+  sa.lse_row = nullptr;
+  sa.tok_row = nullptr;
   sa.err = c->err;
+
+  if (mode == JET_MODE_RESTRICTED) {
+    // restricted head (zeroes the error word), then validation + set rules
+    RestrictedSetArgs rs;
+    RestrictedArgs& ra = rs.r;
+    ra.N = n_rows;
+    ra.d = c->d;
+    ra.V = c->V;
+    ra.n_union = n_union;
+    ra.num_sms = c->num_sms;
+    ra.H = static_cast<const uint16_t*>(H);
+    ra.W = static_cast<const uint16_t*>(W);
+    ra.union_ids = union_ids;
+    ra.zu = (size_t)n_rows * (size_t)n_union <= c->zu_cap ? c->zu : nullptr;
+    ra.lse_row = c->lse_row;
+    ra.lse = o.lse;
+    ra.umap = c->umap;
+    ra.err = c->err;
+    rs.s = sa;
+    rs.n_cand = n_cand;
+    rs.n_tok = n_tok;
+    rs.tok_row = tok_row;
+    rs.kind = kind;
+    {
+      ProfScope ps(c, K_RESTRICTED, st);
+      if (launch_restricted(ra, st) != cudaSuccess) return JET_ERR_CUDA;
+    }
+    ProfScope ps(c, K_SETS, st);
+    return cuda_status(launch_restricted_sets(rs, st));
+  }
+
+  PrepArgs pa;
+  pa.n_rows = n_rows;
+  pa.n_tok = n_tok;
+  pa.V = c->V;
+  pa.tok_row = tok_row;
+  pa.tok_ids = tok_ids;
+  pa.cand_offsets = cand_offsets;
+  pa.n_cand = n_cand;
+  pa.set_offsets = set_offsets;
+  pa.kind = kind;
+  pa.n_sets = n_sets;
+  pa.row_ptr = c->row_ptr;
+  pa.row_cur = c->row_cur;
+  pa.row_list = c->row_list;
+  pa.err = c->err;
+  {
+    ProfScope ps(c, K_PREP, st);
+    if (launch_prep(pa, st) != cudaSuccess) return JET_ERR_CUDA;
+  }
+  const int rc = run_full_head(c, H, W, n_rows, sa.logp, o.lse, c->lse_row, st);
+  if (rc != JET_OK) return rc;
+  sa.zg = c->zg;            // logp = z - lse(row), formed by the set kernel
+  sa.lse_row = c->lse_row;
+  sa.tok_row = tok_row;
   ProfScope ps(c, K_SETS, st);
   return cuda_status(launch_sets(sa, st));
 }
@@ -396,7 +416,11 @@ int jet_create(jet_ctx** out, int d, int V, int max_rows, int max_tokens, int de
   A(dalloc(&c->row_ptr, R + 1));
   A(dalloc(&c->row_cur, R + 1));
   A(dalloc(&c->row_list, Tk));
-  A(dalloc(&c->upos, Tk));
+  A(dalloc(&c->iscratch, Tk));
+  A(dalloc(&c->lse_row, R));
+  A(dalloc(&c->umap, (size_t)V));
+  c->zu_cap = std::max(R * ZU_FLOATS_PER_ROW, ZU_FLOATS_MIN);
+  A(dalloc(&c->zu, c->zu_cap));
   A(dalloc(&c->zg, Tk));
   A(dalloc(&c->part, (size_t)c->units_cap * 2 * BM));
   A(dalloc(&c->hash, Tk));
@@ -439,7 +463,7 @@ void jet_destroy(jet_ctx* c) {
   if (!c) return;
   DeviceGuard g(c->device);
   cudaDeviceSynchronize();
-  void* ptrs[] = {c->err, c->row_ptr, c->row_cur, c->row_list, c->upos, c->zg, c->part, c->hash,
+  void* ptrs[] = {c->err, c->row_ptr, c->row_cur, c->row_list, c->iscratch, c->lse_row, c->umap, c->zu, c->zg, c->part, c->hash,
                   c->lse, c->logp, c->s, c->q, c->qe, c->dec, c->expd, c->conf, c->mass, c->stH,
                   c->st_row, c->st_tok, c->st_co, c->st_so, c->st_kind, c->st_union,
                   c->dd_hash, c->dd_keys, c->dd_vals, c->dd_rep, c->dd_rank};
@@ -516,7 +540,7 @@ int jet_fit_temperature(jet_ctx* c, const float* s, const int32_t* tok_ids, int 
   a.gold = gold;
   a.T_min = T_min;
   a.T_max = T_max;
-  a.flags = reinterpret_cast<uint8_t*>(c->upos);   // [max_tokens] ints of scratch, n_cand bytes used
+  a.flags = reinterpret_cast<uint8_t*>(c->iscratch);   // [max_tokens] ints of scratch, n_cand bytes used
   a.result = c->fit_res;
   a.err = c->err;
   if (launch_fit_temperature(a, st) != cudaSuccess) {
@@ -667,17 +691,15 @@ int jet_score_tokens(jet_ctx* c, const void* H, const void* W, const int32_t* to
   pa.V = c->V;
   pa.tok_row = nullptr;   // token i is predicted by row i
   pa.tok_ids = tok_ids;
-  pa.mode = JET_MODE_FULL;
   pa.row_ptr = c->row_ptr;
   pa.row_cur = c->row_cur;
   pa.row_list = c->row_list;
-  pa.upos = c->upos;
   pa.err = c->err;
   {
     ProfScope ps(c, K_PREP, st);
     if (launch_prep(pa, st) != cudaSuccess) return JET_ERR_CUDA;
   }
-  int rc = run_full_head(c, H, W, n_pos, logp, lse, st);
+  int rc = run_full_head(c, H, W, n_pos, logp, lse, nullptr, st);
   if (rc != JET_OK) {
     cudaStreamSynchronize(st);
     return rc;

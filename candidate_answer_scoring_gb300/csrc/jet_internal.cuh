@@ -142,11 +142,9 @@ struct PrepArgs {
   const int32_t* tok_ids;
   const int32_t* cand_offsets; int n_cand;   // NULL when no sets (jet_score_tokens)
   const int32_t* set_offsets; const uint8_t* kind; int n_sets;
-  int mode; const int32_t* union_ids; int n_union;
   int* row_ptr;    // [n_rows+1]
   int* row_cur;    // [n_rows+1] scratch counters
   int2* row_list;  // [n_tok]
-  int* upos;       // [n_tok] restricted mode: position of the token in the union
   int* err;
 };
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t st);
@@ -156,34 +154,51 @@ cudaError_t launch_head(const CUtensorMap& tmH, const CUtensorMap& tmW, const He
                         cudaStream_t st);
 
 struct MergeArgs {
-  int N; Plan plan;
-  const float2* part; const float* zg;
-  const int* row_ptr; const int2* row_list;
-  float* lse;   // [N] or NULL
-  float* logp;  // [n_tok]
-  const int* err;
+  int N = 0;
+  Plan plan;
+  const float2* part = nullptr;
+  const float* zg = nullptr;
+  float* lse = nullptr;       // [N] or NULL
+  float* lse_row = nullptr;   // [N] per-row lse for the set kernel; NULL: token r of row r,
+  float* logp = nullptr;      //     logp[r] = zg[r] - lse (one token per row)
+  const int* err = nullptr;
 };
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t st);
 
 struct RestrictedArgs {
-  int N, d, n_union;
+  int N, d, V, n_union, num_sms;
   const uint16_t* H; const uint16_t* W; const int32_t* union_ids;
-  const int* row_ptr; const int2* row_list; const int* upos;
-  float* lse; float* logp;
-  const int* err;
+  float* zu;        // [N * n_union] logits over the union, or NULL (recomputed per token)
+  float* lse_row;   // [N] log-sum-exp over the union
+  float* lse;       // [N] caller's output or NULL
+  int* umap;        // [V] union position of a token id (validated against union_ids)
+  int* err;
 };
 cudaError_t launch_restricted(const RestrictedArgs& a, cudaStream_t st);
 
 struct SetArgs {
   int n_sets;
-  const float* logp; const int32_t* tok_ids; const int32_t* cand_offsets;
+  float* logp; const int32_t* tok_ids; const int32_t* cand_offsets;
   const int32_t* set_offsets; float T;
   float* s; float* q; float* q_equiv; int32_t* decision; float* expected;
   float* confidence; float* mass;
   unsigned long long* hash;   // [n_cand] scratch
+  // full-vocabulary path: logp[t] = zg[t] - lse_row[tok_row[t]] is formed (and
+  // stored) while the chain rule runs; NULL zg: logp is read as given
+  const float* zg; const float* lse_row; const int32_t* tok_row;
   const int* err;
 };
 cudaError_t launch_sets(const SetArgs& a, cudaStream_t st);
+
+// Validation, union lookup and set rules of the restricted path (after
+// launch_restricted); n_cand, n_tok, r.N and r.V bound every index it follows.
+struct RestrictedSetArgs {
+  SetArgs s;
+  RestrictedArgs r;
+  int n_cand, n_tok;
+  const int32_t* tok_row; const uint8_t* kind;
+};
+cudaError_t launch_restricted_sets(const RestrictedSetArgs& a, cudaStream_t st);
 
 struct DedupArgs {
   int n_rows, d, n_tok;

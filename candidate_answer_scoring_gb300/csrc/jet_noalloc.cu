@@ -122,11 +122,9 @@ extern "C" int jet_score_tokens_noalloc(const void* H, const void* W, int d, int
   pa.V = V;
   pa.tok_row = nullptr;   // token i is predicted by row i
   pa.tok_ids = tok_ids;
-  pa.mode = JET_MODE_FULL;
   pa.row_ptr = row_ptr;
   pa.row_cur = row_cur;
   pa.row_list = row_list;
-  pa.upos = nullptr;      // full mode only
   pa.err = err;
   if (launch_prep(pa, st) != cudaSuccess) return JET_ERR_CUDA;
 
@@ -157,8 +155,6 @@ extern "C" int jet_score_tokens_noalloc(const void* H, const void* W, int d, int
   ma.plan = ha.plan;
   ma.part = part;
   ma.zg = zg;
-  ma.row_ptr = row_ptr;
-  ma.row_list = row_list;
   ma.lse = lse;
   ma.logp = logp;
   ma.err = err;

@@ -44,21 +44,43 @@ constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;        // 2 s per wa
 constexpr unsigned long long EXIT_LIMIT_NS = 3 * WAIT_LIMIT_NS;    // pair exit handshake
 
 // ---- TMA ----------------------------------------------------------------------
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+// Every load carries an L2 eviction policy (createpolicy): W tiles that no
+// other CTA reads are marked evict-first so that the stream of W does not push
+// the row tiles, the partials and the small per-call arrays out of L2; the H
+// tiles of the band are marked evict-last.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                            uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
       : "memory");
 }
 
 // Paired form: the copy lands in this CTA's shared memory and completes on
 // the barrier at cluster address `bar` (the issuing CTA's barrier).
-__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, int x, int y, uint32_t bar,
+                                                 uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "l"(policy)
       : "memory");
 }
 
@@ -263,7 +285,10 @@ __global__ void __launch_bounds__(HEAD_THREADS, 1)
   const bool issuer = rank == 0;
   const int unit0 = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
   const int unit_step = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
-  pdl_trigger();   // the merge kernel may be scheduled; it waits for this grid to finish
+  // No early launch_dependents here: the merge kernel is launched when this
+  // grid completes.  Launched early, its CTAs pile onto the SMs the head
+  // leaves free and run there several times slower than when spread over all
+  // SMs after the head (measured on GB300).
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NST; ++i) {
@@ -297,6 +322,9 @@ __global__ void __launch_bounds__(HEAD_THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued_mask = 0, issued_parity = 0;   // per stage: has a load, parity of its phase
+      // one row tile: each W tile is read by this CTA (pair) alone
+      const uint64_t pol_w = P.n_mt == 1 ? l2_policy_evict_first() : l2_policy_evict_normal();
+      const uint64_t pol_h = l2_policy_evict_last();
       bool ok = true;
       for (int u = unit0; ok && u < P.units; u += unit_step) {
         int m, vt0, vt1;
@@ -310,12 +338,12 @@ __global__ void __launch_bounds__(HEAD_THREADS, 1)
             if constexpr (PAIR) {
               if (issuer) mbar_arrive_expect_tx(&full[stage], 2 * SH::STAGE_BYTES);   // both CTAs' halves
               const uint32_t bar = cluster_addr(&full[stage], 0);
-              tma_load_2d_pair(sA + stage * SH::A_BYTES, &tmH, kb * BK, a_row, bar);
-              tma_load_2d_pair(sB + stage * SH::B_BYTES, &tmW, kb * BK, b_row, bar);
+              tma_load_2d_pair(sA + stage * SH::A_BYTES, &tmH, kb * BK, a_row, bar, pol_h);
+              tma_load_2d_pair(sB + stage * SH::B_BYTES, &tmW, kb * BK, b_row, bar, pol_w);
             } else {
               mbar_arrive_expect_tx(&full[stage], SH::STAGE_BYTES);
-              tma_load_2d(sA + stage * SH::A_BYTES, &tmH, kb * BK, a_row, &full[stage]);
-              tma_load_2d(sB + stage * SH::B_BYTES, &tmW, kb * BK, b_row, &full[stage]);
+              tma_load_2d(sA + stage * SH::A_BYTES, &tmH, kb * BK, a_row, &full[stage], pol_h);
+              tma_load_2d(sB + stage * SH::B_BYTES, &tmW, kb * BK, b_row, &full[stage], pol_w);
             }
             if (a.pf_kblocks > 0) {   // optional: more W bytes in flight than the ring holds
               const int ip = (vt - vt0) * kblocks + kb + a.pf_kblocks;

@@ -1,6 +1,8 @@
-// Device pre-pass: validates every index the rest of the path will use and
+// Device pre-pass of the full-vocabulary path: validates every index the rest
+// of the path will use and
 // builds, per hidden row, the list of scored tokens it predicts (sorted by
-// token id), which the head's epilogue walks while it sweeps vocabulary tiles.
+// token id), which the head's epilogue walks while it sweeps vocabulary
+// tiles.
 // Three layouts: one token per row (jet_score_tokens), tokens already grouped
 // by row (tok_row non-decreasing: row pointers from run boundaries), and the
 // general case (count, scan, scatter).
@@ -21,18 +23,19 @@ __device__ __forceinline__ int row_of(const PrepArgs& a, int j) {
   return a.tok_row ? a.tok_row[j] : j;
 }
 
-// Dynamic shared memory: [n_union] union ids (restricted mode), then
-// [n_rows + 1] per-row counters when SMEM_COUNTS.  Kept small so that the
-// head kernel's CTA can share an SM with this one while it starts.
+// Dynamic shared memory: [n_rows + 1] per-row counters when SMEM_COUNTS.
+// Kept small so that the head kernel's CTA can share an SM with this one.
 template <bool SMEM_COUNTS>
 __global__ void __launch_bounds__(PREP_THREADS) prep_kernel(PrepArgs a) {
-  extern __shared__ int s_dyn[];
+  extern __shared__ int s_cnt[];
   __shared__ int s_warp[PREP_THREADS / 32];
   __shared__ int s_unsorted;
-  int* s_union = s_dyn;
-  int* s_cnt = s_dyn + (a.mode == JET_MODE_RESTRICTED ? a.n_union : 0);
   const int tid = threadIdx.x, nth = blockDim.x, lane = tid & 31, warp = tid >> 5;
-  pdl_trigger();   // the head may start its loads and MMAs; it waits before reading our outputs
+  // Everything earlier on the stream has finished (and its writes are visible)
+  // before this kernel touches memory, and before the head may start: the head
+  // streams H and W as soon as it is scheduled and waits only for our outputs.
+  pdl_wait();
+  pdl_trigger();
   int* err = a.err;
   int* cnt = SMEM_COUNTS ? s_cnt : a.row_cur;
   const bool identity = a.tok_row == nullptr;    // token i is predicted by row i
@@ -41,8 +44,6 @@ __global__ void __launch_bounds__(PREP_THREADS) prep_kernel(PrepArgs a) {
     for (int i = 0; i < ERR_WORDS; ++i) err[i] = 0;
     s_unsorted = 0;
   }
-  if (a.mode == JET_MODE_RESTRICTED)
-    for (int u = tid; u < a.n_union; u += nth) s_union[u] = a.union_ids[u];
   __syncthreads();
 
   // scored tokens: id in [0, V), row in [0, n_rows); is tok_row non-decreasing?
@@ -61,7 +62,6 @@ __global__ void __launch_bounds__(PREP_THREADS) prep_kernel(PrepArgs a) {
     for (int c = tid; c < a.n_cand; c += nth) {
       const int len = a.cand_offsets[c + 1] - a.cand_offsets[c];
       if (len < 1) set_error(err, JET_ERR_OFFSETS, c);
-      else if (a.mode == JET_MODE_RESTRICTED && len != 1) set_error(err, JET_ERR_MODE, c);
     }
     for (int k = tid; k < a.n_sets; k += nth) {
       const int K = a.set_offsets[k + 1] - a.set_offsets[k];
@@ -73,25 +73,6 @@ __global__ void __launch_bounds__(PREP_THREADS) prep_kernel(PrepArgs a) {
     }
   }
 
-  // restricted mode: union ids in range and distinct; every token in the union
-  if (a.mode == JET_MODE_RESTRICTED) {
-    for (int u = tid; u < a.n_union; u += nth) {
-      const int t = s_union[u];
-      if (t < 0 || t >= a.V) set_error(err, JET_ERR_TOKEN_RANGE, u);
-    }
-    __syncthreads();                                 // range errors take precedence
-    for (int u = tid; u < a.n_union; u += nth)
-      for (int w = 0; w < u; ++w)
-        if (s_union[w] == s_union[u]) set_error(err, JET_ERR_NOT_IN_UNION, u);
-    for (int j = tid; j < a.n_tok; j += nth) {
-      const int t = a.tok_ids[j];
-      int pos = -1;
-      for (int u = 0; u < a.n_union; ++u)
-        if (s_union[u] == t) pos = u;
-      if (pos < 0) set_error(err, JET_ERR_NOT_IN_UNION, j);
-      a.upos[j] = pos;
-    }
-  }
   __syncthreads();
   if (*(volatile int*)err != 0) return;
 
@@ -194,12 +175,9 @@ __global__ void __launch_bounds__(PREP_THREADS) prep_kernel(PrepArgs a) {
 }  // namespace
 
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t st) {
-  const size_t union_bytes = (a.mode == JET_MODE_RESTRICTED ? (size_t)a.n_union : 0) * sizeof(int);
   if (a.tok_row != nullptr && a.n_rows + 1 <= PREP_SMEM_ROWS)
-    prep_kernel<true><<<1, PREP_THREADS, union_bytes + (a.n_rows + 1) * sizeof(int), st>>>(a);
-  else
-    prep_kernel<false><<<1, PREP_THREADS, union_bytes, st>>>(a);
-  return cudaGetLastError();
+    return launch_dependent(prep_kernel<true>, dim3(1), dim3(PREP_THREADS), (a.n_rows + 1) * sizeof(int), st, a);
+  return launch_dependent(prep_kernel<false>, dim3(1), dim3(PREP_THREADS), 0, st, a);
 }
 
 }  // namespace jet

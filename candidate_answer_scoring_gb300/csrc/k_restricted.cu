@@ -9,24 +9,41 @@
 // The set rules then run unchanged; within a set sharing one row, lse_U
 // cancels and q = softmax(z / T) over the set's codes (step 6).
 //
-// Work is tiny (|U| is tens of codes) and latency-bound, so the kernel
-// spreads it wide: one CTA of 32 warps per hidden row, one code per warp at a
-// time.  Lane l multiplies 16-byte bf16 vectors l, l+32, ... of the row and
-// of the code's embedding row (the union rows stay L2-resident across CTAs),
-// loading up to 4 vector pairs before using them, and a fixed butterfly
-// finishes each dot product, so identical rows give bit-identical logits.
-// z_U lives in shared memory; the CTA then takes lse_U and writes the
-// log-probability of each of the row's tokens.
+// The work is tiny (|U| is tens of codes) and latency-bound, so the path is
+// two launches with few dependent memory round trips each:
+//
+//  1. restricted_head_kernel: z = H U^T is a small dense contraction, run on
+//     the tensor cores with mma.sync (m16n8k16, bf16 in, fp32 accumulate).
+//     One CTA per 16 rows; its 16 warps split d, each accumulating the
+//     16 x 32 tile of a group of 32 codes, and the warps' partials are summed
+//     in a fixed order through shared memory.  Warp r then folds row r's 32
+//     logits into a running (max, sum) for lse_U.  z goes to an [N, |U|]
+//     scratch when that fits the context's workspace, else the second kernel
+//     recomputes the few logits it needs (a warp dot product: the same bf16
+//     products in fp32, summed in another order).  CTA 0 zeroes the error word
+//     and records each union id's position in a token-id map.  This kernel
+//     validates nothing and reads only rows < N and union rows whose id lies
+//     in [0, V).
+//  2. restricted_sets_kernel, one warp per set: checks the set's offsets and
+//     kind, that each candidate is one token whose id and row are in range and
+//     whose id the map places in the union (the map is trusted only where
+//     union_ids agrees, so stale entries from earlier calls are harmless),
+//     forms logp, then runs the set rules.  Warp 0 of CTA 0 checks the ends of
+//     the offset arrays and that the union ids are in range and distinct.
 #include <cuda_bf16.h>
 
 #include "jet_internal.cuh"
+#include "jet_setrules.cuh"
 
 namespace jet {
 namespace {
 
-constexpr int RT_THREADS = 1024;  // 32 warps
-constexpr int RT_WARPS = RT_THREADS / 32;
-constexpr int RT_BATCH = 4;       // 16-byte vector pairs in flight per lane (64-register budget)
+constexpr int RT_WARPS = 16;                  // warps of the restricted head, splitting d
+constexpr int RT_THREADS = RT_WARPS * 32;     // = 16 rows x 32 codes for the reduction
+constexpr int RT_CODES = 32;                  // codes per group: four n8 tiles
+constexpr int RT_UNROLL = 3;                  // 32-wide k chunks with loads in flight per warp
+constexpr int DR_BATCH = 10;                  // 16-byte vectors in flight per lane (warp dot product)
+constexpr int RS_WARPS = 8;                   // sets per CTA of the set kernel
 
 __device__ __forceinline__ float dot_bf16x8(uint4 h, uint4 w, float acc) {
   const __nv_bfloat162* hp = reinterpret_cast<const __nv_bfloat162*>(&h);
@@ -41,71 +58,276 @@ __device__ __forceinline__ float dot_bf16x8(uint4 h, uint4 w, float acc) {
   return acc;
 }
 
-__global__ void __launch_bounds__(RT_THREADS) restricted_kernel(const RestrictedArgs a) {
-  __shared__ float sZ[JET_MAX_UNION];
-  __shared__ float sRed[2 * RT_WARPS];
-  pdl_trigger();
-  pdl_wait();
-  if (*(volatile const int*)a.err != 0) return;
-  const int r = blockIdx.x;
-  const int U = a.n_union;
-  const int nvec = a.d / 8;                             // 16-byte vectors per row
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint4* h = reinterpret_cast<const uint4*>(a.H) + (size_t)r * nvec;
-  const uint4* Wv = reinterpret_cast<const uint4*>(a.W);
-
-  for (int u = warp; u < U; u += RT_WARPS) {
-    const uint4* w = Wv + (size_t)a.union_ids[u] * nvec;
-    float acc = 0.f;
-    for (int k0 = lane; k0 < nvec; k0 += 32 * RT_BATCH) {
-      uint4 hv[RT_BATCH], wv[RT_BATCH];
+// h . w over nvec 16-byte bf16 vectors by one warp (lane l takes vectors l,
+// l+32, ...; a fixed butterfly combines the lanes; every lane gets the sum).
+__device__ __forceinline__ float dot_row(const uint4* h, const uint4* w, int nvec, int lane) {
+  float acc = 0.f;
+  for (int k0 = lane; k0 < nvec; k0 += 32 * DR_BATCH) {
+    uint4 hv[DR_BATCH / 2], wv[DR_BATCH / 2];
+    for (int half = 0; half < 2; ++half) {
+      const int kb = k0 + 32 * (DR_BATCH / 2) * half;
 #pragma unroll
-      for (int i = 0; i < RT_BATCH; ++i) {
-        const int k = k0 + 32 * i;
+      for (int i = 0; i < DR_BATCH / 2; ++i) {
+        const int k = kb + 32 * i;
         if (k < nvec) { hv[i] = h[k]; wv[i] = w[k]; }
       }
 #pragma unroll
-      for (int i = 0; i < RT_BATCH; ++i)
-        if (k0 + 32 * i < nvec) acc = dot_bf16x8(hv[i], wv[i], acc);
+      for (int i = 0; i < DR_BATCH / 2; ++i)
+        if (kb + 32 * i < nvec) acc = dot_bf16x8(hv[i], wv[i], acc);
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) sZ[u] = acc;
   }
-  __syncthreads();
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  return acc;
+}
 
-  // lse over the union: block max, then block sum of exp(z - max)
-  float M = -INFINITY;
-  for (int u = threadIdx.x; u < U; u += RT_THREADS) M = fmaxf(M, sZ[u]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  if (lane == 0) sRed[warp] = M;
-  __syncthreads();
-  M = sRed[0];
-#pragma unroll
-  for (int i = 1; i < RT_WARPS; ++i) M = fmaxf(M, sRed[i]);
-  float sum = 0.f;
-  for (int u = threadIdx.x; u < U; u += RT_THREADS) sum += expf(sZ[u] - M);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-  if (lane == 0) sRed[RT_WARPS + warp] = sum;
-  __syncthreads();
-  sum = 0.f;
-#pragma unroll
-  for (int i = 0; i < RT_WARPS; ++i) sum += sRed[RT_WARPS + i];
-  const float lse = M + logf(sum);
-  if (threadIdx.x == 0 && a.lse) a.lse[r] = lse;
-  for (int e = a.row_ptr[r] + threadIdx.x; e < a.row_ptr[r + 1]; e += RT_THREADS) {
-    const int j = a.row_list[e].y;
-    a.logp[j] = sZ[a.upos[j]] - lse;
+// D += A B for one m16n8k16 tile: A 16x16 bf16 (row-major fragments), B 16x8
+// bf16 (column-major fragments), D 16x8 fp32.
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Fragment mapping.  In an m16n8k16 MMA, lane (g = lane/4, c = lane%4) holds
+// A elements (rows g and g+8) and B elements (code g) at k slots {2c, 2c+1,
+// 2c+8, 2c+9}.  A dot product does not care which physical k feeds which slot
+// as long as A and B agree, so slots {2c, 2c+1} take physical k = 4c, 4c+1 and
+// slots {2c+8, 2c+9} take 4c+2, 4c+3: each lane then reads 4 consecutive
+// elements per row and step, and one 16-byte load per row serves two steps of
+// a 32-wide chunk (words 0-1: step 0, words 2-3: step 1).
+__global__ void __launch_bounds__(RT_THREADS, 1) restricted_head_kernel(const RestrictedArgs a) {
+  __shared__ float sAcc[RT_WARPS][16][RT_CODES + 1];
+  __shared__ float sM[16], sS[16];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, c = lane & 3;
+  const int U = a.n_union, d = a.d;
+  const int r0 = blockIdx.x * 16;
+  pdl_wait();      // earlier work on the stream is complete before any access
+  pdl_trigger();
+  if (blockIdx.x == 0) {
+    if (tid < ERR_WORDS) a.err[tid] = 0;
+    for (int u = tid; u < U; u += RT_THREADS) {
+      const int t = a.union_ids[u];
+      if (t >= 0 && t < a.V) a.umap[t] = u;
+    }
   }
+  if (tid < 16) { sM[tid] = -INFINITY; sS[tid] = 0.f; }
+
+  // this lane's two rows (clamped to the last row: loads stay in bounds, the
+  // results of rows past N are never written)
+  const int nch = d / 32;                                    // 32-wide k chunks
+  const int ch0 = warp * nch / RT_WARPS, ch1 = (warp + 1) * nch / RT_WARPS;
+  const uint4* hA = reinterpret_cast<const uint4*>(a.H + (size_t)min(r0 + g, a.N - 1) * d) + c;
+  const uint4* hB = reinterpret_cast<const uint4*>(a.H + (size_t)min(r0 + g + 8, a.N - 1) * d) + c;
+
+  for (int u0 = 0; u0 < U; u0 += RT_CODES) {
+    const uint4* wr[4];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      const int u = u0 + nt * 8 + g;
+      const int t = u < U ? a.union_ids[u] : -1;
+      wr[nt] = reinterpret_cast<const uint4*>(a.W + (size_t)((t >= 0 && t < a.V) ? t : 0) * d) + c;
+    }
+    float acc[4][4];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[nt][i] = 0.f;
+    for (int ch = ch0; ch < ch1; ch += RT_UNROLL) {
+      uint4 A0[RT_UNROLL], A1[RT_UNROLL], B[RT_UNROLL][4];
+#pragma unroll
+      for (int j = 0; j < RT_UNROLL; ++j) {
+        if (ch + j < ch1) {
+          const int v = (ch + j) * 4;                         // 16-byte vectors per chunk: 4 per row
+          A0[j] = hA[v];
+          A1[j] = hB[v];
+#pragma unroll
+          for (int nt = 0; nt < 4; ++nt) B[j][nt] = wr[nt][v];
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < RT_UNROLL; ++j) {
+        if (ch + j < ch1) {
+#pragma unroll
+          for (int nt = 0; nt < 4; ++nt) {
+            mma_bf16_16816(acc[nt], A0[j].x, A1[j].x, A0[j].y, A1[j].y, B[j][nt].x, B[j][nt].y);
+            mma_bf16_16816(acc[nt], A0[j].z, A1[j].z, A0[j].w, A1[j].w, B[j][nt].z, B[j][nt].w);
+          }
+        }
+      }
+    }
+    // partial tiles to shared memory: (row g | g+8, code nt*8 + 2c | +1)
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      sAcc[warp][g][nt * 8 + 2 * c] = acc[nt][0];
+      sAcc[warp][g][nt * 8 + 2 * c + 1] = acc[nt][1];
+      sAcc[warp][g + 8][nt * 8 + 2 * c] = acc[nt][2];
+      sAcc[warp][g + 8][nt * 8 + 2 * c + 1] = acc[nt][3];
+    }
+    __syncthreads();
+    // warp w now owns row w of the tile, lane = code: sum the warps' partials
+    // in order, store z, fold the group into the row's running (max, sum)
+    {
+      const int row = warp, u = u0 + lane, r = r0 + row;
+      float z = 0.f;
+#pragma unroll
+      for (int w = 0; w < RT_WARPS; ++w) z += sAcc[w][row][lane];
+      bool valid = u < U;
+      if (valid) {
+        const int t = a.union_ids[u];
+        if (!(t >= 0 && t < a.V)) z = __int_as_float(0x7fc00000);   // reported by the set kernel
+        if (a.zu && r < a.N) a.zu[(size_t)r * U + u] = z;
+      }
+      float m = valid ? z : -INFINITY;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      const float M = fmaxf(sM[row], m);
+      float e = valid ? expf(z - M) : 0.f;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) e += __shfl_xor_sync(0xffffffffu, e, o);
+      if (lane == 0) {
+        sS[row] = (sM[row] == -INFINITY ? 0.f : sS[row] * expf(sM[row] - M)) + e;
+        sM[row] = M;
+      }
+    }
+    __syncthreads();   // sAcc is reused by the next group
+  }
+  if (lane == 0 && r0 + warp < a.N) {
+    const float lse = sM[warp] + logf(sS[warp]);
+    a.lse_row[r0 + warp] = lse;
+    if (a.lse) a.lse[r0 + warp] = lse;
+  }
+}
+
+// Candidate c of a restricted set: one token, id and row in range, id in the
+// union.  Returns false (after recording the error) otherwise; with the
+// union-logit scratch, also forms and stores the token's logp.
+__device__ __forceinline__ bool restricted_candidate(const RestrictedSetArgs& a, int c, int& tok, float& lp) {
+  const SetArgs& sa = a.s;
+  const RestrictedArgs& ra = a.r;
+  int* err = ra.err;
+  const int t0 = sa.cand_offsets[c], t1 = sa.cand_offsets[c + 1];
+  if (!(t0 >= 0 && t0 < t1 && t1 <= a.n_tok)) { set_error(err, JET_ERR_OFFSETS, c); return false; }
+  if (t1 - t0 != 1) { set_error(err, JET_ERR_MODE, c); return false; }
+  const int t = sa.tok_ids[t0], r = a.tok_row[t0];
+  if (t < 0 || t >= ra.V || r < 0 || r >= ra.N) { set_error(err, JET_ERR_TOKEN_RANGE, t0); return false; }
+  const int pos = ra.umap[t];
+  const float lse = ra.lse_row[r];
+  if (pos < 0 || pos >= ra.n_union) { set_error(err, JET_ERR_NOT_IN_UNION, t0); return false; }
+  const int uid = ra.union_ids[pos];
+  const float z = ra.zu ? ra.zu[(size_t)r * ra.n_union + pos] : 0.f;
+  if (uid != t) { set_error(err, JET_ERR_NOT_IN_UNION, t0); return false; }   // a stale map entry
+  tok = t;
+  lp = z - lse;
+  if (ra.zu) sa.logp[t0] = lp;
+  return true;
+}
+
+// Sets of K <= 32*CPL candidates with the scratch: scores straight from the
+// candidates' logp (s(c) = logp of its one token), rules in registers.
+template <int CPL>
+__device__ __forceinline__ void restricted_set_regs(const RestrictedSetArgs& a, int set, int lane, int c0, int K) {
+  float sc[CPL];
+  unsigned long long h[CPL];
+  bool bad = false;
+#pragma unroll
+  for (int k = 0; k < CPL; ++k) {
+    const int i = k * 32 + lane;
+    sc[k] = -INFINITY;
+    h[k] = 0;
+    if (i < K) {
+      int tok;
+      float lp;
+      if (restricted_candidate(a, c0 + i, tok, lp)) {
+        sc[k] = 0.f + lp;                 // the chain rule over one token
+        h[k] = single_token_hash(tok);
+      } else {
+        bad = true;
+      }
+    }
+  }
+  if (__any_sync(0xffffffffu, bad)) return;
+  set_rules_core<CPL>(a.s, set, lane, c0, K, 1.0f / a.s.T, sc, h);
+}
+
+__global__ void __launch_bounds__(32 * RS_WARPS) restricted_sets_kernel(const RestrictedSetArgs a) {
+  const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int k = blockIdx.x * RS_WARPS + wib;
+  const SetArgs& sa = a.s;
+  const RestrictedArgs& ra = a.r;
+  int* err = ra.err;
+  const int U = ra.n_union;
+  pdl_wait();
+  pdl_trigger();
+  if (blockIdx.x == 0 && wib == 0) {
+    if (lane == 0) {
+      if (sa.set_offsets[0] != 0 || sa.set_offsets[sa.n_sets] != a.n_cand) set_error(err, JET_ERR_OFFSETS, 0);
+      if (sa.cand_offsets[0] != 0 || sa.cand_offsets[a.n_cand] != a.n_tok) set_error(err, JET_ERR_OFFSETS, 0);
+    }
+    for (int u = lane; u < U; u += 32) {
+      const int t = ra.union_ids[u];
+      if (t < 0 || t >= ra.V) set_error(err, JET_ERR_TOKEN_RANGE, u);
+      else if (ra.umap[t] != u) set_error(err, JET_ERR_NOT_IN_UNION, u);   // a repeated id keeps one position
+    }
+  }
+  if (k >= sa.n_sets) return;
+
+  // the set's own offsets and kind (consecutive sets share a boundary, so
+  // with both ends checked above the sets tile [0, n_cand) exactly)
+  const int c0 = sa.set_offsets[k], c1 = sa.set_offsets[k + 1];
+  const int kd = a.kind[k];
+  if (!(c0 >= 0 && c0 < c1 && c1 <= a.n_cand)) {
+    if (lane == 0) set_error(err, JET_ERR_OFFSETS, k);
+    return;
+  }
+  const int K = c1 - c0;
+  if (kd > JET_KIND_ORDINAL || (kd == JET_KIND_BINARY && K != 2) || (kd == JET_KIND_ORDINAL && K < 2)) {
+    if (lane == 0) set_error(err, kd > JET_KIND_ORDINAL ? JET_ERR_ARG : JET_ERR_OFFSETS, k);
+    return;
+  }
+  if (ra.zu && K <= 128) {
+    if (K <= 32) restricted_set_regs<1>(a, k, lane, c0, K);
+    else if (K <= 64) restricted_set_regs<2>(a, k, lane, c0, K);
+    else restricted_set_regs<4>(a, k, lane, c0, K);
+    return;
+  }
+
+  // large sets, or no scratch: logp through global memory, then the general rules
+  bool bad = false;
+  for (int c = c0 + lane; c < c1; c += 32) {
+    int tok;
+    float lp;
+    if (!restricted_candidate(a, c, tok, lp)) bad = true;
+  }
+  if (__any_sync(0xffffffffu, bad)) return;
+  if (!ra.zu) {   // no scratch: the warp recomputes each candidate's logit
+    const int nvec = ra.d / 8;
+    for (int c = c0; c < c1; ++c) {
+      const int t0 = sa.cand_offsets[c];
+      const int t = sa.tok_ids[t0], r = a.tok_row[t0];
+      const float z = dot_row(reinterpret_cast<const uint4*>(ra.H) + (size_t)r * nvec,
+                              reinterpret_cast<const uint4*>(ra.W) + (size_t)t * nvec, nvec, lane);
+      if (lane == 0) sa.logp[t0] = z - ra.lse_row[r];
+    }
+  }
+  __syncwarp();    // logp written by any lane is visible to the whole warp
+  set_rules_warp(sa, k, lane, c0, c1);
 }
 
 }  // namespace
 
 cudaError_t launch_restricted(const RestrictedArgs& a, cudaStream_t st) {
   if (a.N <= 0) return cudaSuccess;
-  return launch_dependent(restricted_kernel, dim3(a.N), dim3(RT_THREADS), 0, st, a);
+  return launch_dependent(restricted_head_kernel, dim3((a.N + 15) / 16), dim3(RT_THREADS), 0, st, a);
+}
+
+cudaError_t launch_restricted_sets(const RestrictedSetArgs& a, cudaStream_t st) {
+  if (a.s.n_sets <= 0) return cudaSuccess;
+  return launch_dependent(restricted_sets_kernel, dim3((a.s.n_sets + RS_WARPS - 1) / RS_WARPS),
+                          dim3(32 * RS_WARPS), 0, st, a);
 }
 
 }  // namespace jet

@@ -121,6 +121,22 @@ def test_restricted_mode_checks(env):
     still_works(sc, wl)
 
 
+def test_restricted_mode_ranges_and_offsets(env):
+    """The restricted path validates in its own set kernel: same status codes."""
+    jet, sc, wl, rest = env
+    t = rest.tok_ids.copy(); t[3] = rest.V
+    assert call(sc, args_of(rest, tok_ids=dev(t))) == TOKEN
+    r = rest.tok_row.copy(); r[0] = rest.N
+    assert call(sc, args_of(rest, tok_row=dev(r))) == TOKEN
+    so = rest.set_offsets.copy(); so[-1] -= 1                             # sets do not cover candidates
+    assert call(sc, args_of(rest, set_offsets=dev(so))) == OFFSETS
+    co = rest.cand_offsets.copy(); co[-1] += 1                            # candidates do not cover tokens
+    assert call(sc, args_of(rest, cand_offsets=dev(co))) == OFFSETS
+    kd = rest.kind.copy(); kd[2] = 9
+    assert call(sc, args_of(rest, kind=dev(kd))) == ARG
+    still_works(sc, rest)
+
+
 def test_score_tokens_checks(env):
     jet, sc, wl, _ = env
     a = args_of(wl)

@@ -105,8 +105,9 @@ def test_restricted_parity(jet):
 
 
 def test_restricted_union_larger_than_one_chunk(jet):
-    """Single-token sets over a 600-code union, d=1024: the union is staged in
-    several shared-memory chunks; rows shared by all codes of a set."""
+    """Single-token sets over a 600-code union, d=1024: the restricted head
+    runs 19 groups of 32 codes (the last one ragged); rows shared by all codes
+    of a set."""
     rng = np.random.default_rng(5)
     d, V = 1024, 20000
     union = rng.choice(V, size=600, replace=False).astype(np.int32)
@@ -120,6 +121,48 @@ def test_restricted_union_larger_than_one_chunk(jet):
     gpu = run_gpu(jet, wl)
     orc = oracle.score_workload(wl)
     compare(wl, gpu, orc)
+
+
+def test_restricted_without_union_logit_scratch(jet):
+    """N x |U| above the context's union-logit scratch (max(128 max_rows, 2^20)
+    floats): the set kernel recomputes each scored logit with the head's dot
+    product.  300 rows (one per set) x a 4000-code union, d=128."""
+    rng = np.random.default_rng(17)
+    d, V, n_union = 128, 6000, 4000
+    union = rng.choice(V, size=n_union, replace=False).astype(np.int32)
+    sets = []
+    for _ in range(300):
+        K = int(rng.integers(2, 7))
+        sets.append(wk._SetSpec(wk.KIND_CHOICE, [(int(t),) for t in rng.choice(union, size=K, replace=False)]))
+    W = wk.gen_W(4321, V, d)
+    wl = wk._build("restricted-4000", 4321, d, V, W, sets, 1.3, row_mode="per_key")
+    wl = wl.with_mode(wk.MODE_RESTRICTED, 1.3, union)
+    assert wl.N * n_union > max(128 * wl.N, 1 << 20)
+    gpu = run_gpu(jet, wl)
+    orc = oracle.score_workload(wl)
+    compare(wl, gpu, orc)
+    # the same sets through the scratch (a union cut to the codes in use) agree
+    used = np.unique(wl.tok_ids).astype(np.int32)
+    small = run_gpu(jet, wl.with_mode(wk.MODE_RESTRICTED, 1.3, used))
+    orc_small = oracle.score_workload(wl.with_mode(wk.MODE_RESTRICTED, 1.3, used))
+    compare(wl.with_mode(wk.MODE_RESTRICTED, 1.3, used), small, orc_small)
+
+
+def test_restricted_wide_rows(jet):
+    """d = 16384, 300 rows (a ragged last tile of 16): each of the restricted
+    head's 16 warps takes 32 of the 512 chunks of d."""
+    rng = np.random.default_rng(23)
+    d, V = 16384, 700
+    union = rng.choice(V, size=120, replace=False).astype(np.int32)
+    sets = []
+    for _ in range(300):
+        K = int(rng.integers(2, 6))
+        sets.append(wk._SetSpec(wk.KIND_CHOICE, [(int(t),) for t in rng.choice(union, size=K, replace=False)]))
+    W = wk.gen_W(777, V, d)
+    wl = wk._build("restricted-wide", 777, d, V, W, sets, 0.9, row_mode="per_key")
+    wl = wl.with_mode(wk.MODE_RESTRICTED, 0.9, union)
+    gpu = run_gpu(jet, wl)
+    compare(wl, gpu, oracle.score_workload(wl))
 
 
 def test_full_equals_restricted_when_union_is_vocab(jet):
