@@ -269,6 +269,19 @@ def gpu_arm(args, world, rank, local):
                         union_ids=None if s.union_ids is None else t(s.union_ids), T=s.T, mode=s.mode, wl=s))
     sc = jet.JetScorer(wl.d, wl.V, wl.N, wl.n_tok, device=local)
     outs = [sc.alloc_outputs(s.N, s.n_tok, s.n_cand, s.n_sets) for s in steps_wl]
+    if args.gather_rows:
+        # rows read in place from a right-padded [N, L, d] source at each
+        # sequence's last valid position (lengths uniform in 1..L)
+        L = args.gather_rows
+        grng = np.random.default_rng(20261202 + 77)
+        lengths = grng.integers(1, L + 1, size=wl.N)
+        from workloads import to_bf16_bits as wk_to_bf16
+        src = wk_to_bf16(grng.standard_normal((wl.N * L, wl.d)).astype(np.float32))
+        row_index = (np.arange(wl.N) * L + lengths - 1).astype(np.int32)
+        src[row_index] = wl.H
+        for x in ins:
+            x["H_src"] = t(src.view(np.int16)).view(torch.bfloat16)
+            x["row_index"] = t(row_index)
     stream = torch.cuda.Stream(dev)
     n_rows_scored = wl.N
     if args.dedup:
@@ -282,6 +295,11 @@ def gpu_arm(args, world, rank, local):
             H, tok_row = x["H"], x["tok_row"]
             if args.dedup:
                 H, tok_row, _ = sc.dedup_rows(H, tok_row, H_unique=Hu_buf[i])
+            if args.gather_rows:
+                sc.score_sets_gather(x["H_src"], x["row_index"], Wd, tok_row, x["tok_ids"], x["cand_offsets"],
+                                     x["set_offsets"], x["kind"], x["T"], x["mode"], x["union_ids"], out=o,
+                                     sync=False)
+                continue
             sc.score_sets(H, Wd, tok_row, x["tok_ids"], x["cand_offsets"], x["set_offsets"], x["kind"],
                           x["T"], x["mode"], x["union_ids"], out=o, sync=False)
 
@@ -369,6 +387,8 @@ def gpu_arm(args, world, rank, local):
             "accumulate": "fp32 (tcgen05 bf16 x bf16 -> fp32 TMEM)",
             "plan": sc.plan_info(n_rows_scored),
             "row_dedup": bool(args.dedup), "rows_scored": n_rows_scored,
+            "row_gather": (f"rows read in place from a right-padded [N, {args.gather_rows}, d] source "
+                           "(TMA gathers)") if args.gather_rows else None,
             "step_roofline_us": t_roof * 1e6, "step_roofline_frac": t_roof / (ms_step / 1e3),
             "kernel_ms_per_step": {k: v["ms"] / K for k, v in prof.items() if isinstance(v, dict)},
             "ms_per_step_with_kernel_events": ms_prof / K,
@@ -534,6 +554,8 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="binary", choices=sorted(WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--gather-rows", type=int, default=0, metavar="L",
+                    help="read H in place from a right-padded [N, L, d] source (jet_score_sets_gather)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--dedup", action="store_true",
                     help="score each distinct hidden row once (jet_dedup_rows before every step)")

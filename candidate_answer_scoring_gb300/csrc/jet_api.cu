@@ -269,7 +269,8 @@ int check_sets_args(jet_ctx* c, const void* H, const void* W, int n_rows, const 
 int score_sets_enqueue(jet_ctx* c, const void* H, const void* W, int n_rows, const int32_t* tok_row,
                        const int32_t* tok_ids, int n_tok, const int32_t* cand_offsets, int n_cand,
                        const int32_t* set_offsets, const uint8_t* kind, int n_sets, float T, int mode,
-                       const int32_t* union_ids, int n_union, const jet_set_out* out, cudaStream_t st) {
+                       const int32_t* union_ids, int n_union, const jet_set_out* out, cudaStream_t st,
+                       const int32_t* row_index = nullptr, int n_src = 0) {
   jet_set_out o;
   std::memset(&o, 0, sizeof o);
   if (out) o = *out;
@@ -306,6 +307,8 @@ int score_sets_enqueue(jet_ctx* c, const void* H, const void* W, int n_rows, con
     ra.H = static_cast<const uint16_t*>(H);
     ra.W = static_cast<const uint16_t*>(W);
     ra.union_ids = union_ids;
+    ra.row_index = row_index;
+    ra.n_src = n_src;
     ra.zu = (size_t)n_rows * (size_t)n_union <= c->zu_cap ? c->zu : nullptr;
     ra.lse_row = c->lse_row;
     ra.lse = o.lse;
@@ -324,10 +327,19 @@ int score_sets_enqueue(jet_ctx* c, const void* H, const void* W, int n_rows, con
     return cuda_status(launch_restricted_sets(rs, st));
   }
 
+  if (row_index) {
+    // gathered rows: compact copy for the head's tiled loads (staging buffer)
+    ProfScope ps(c, K_PREP, st);
+    if (launch_gather_rows(static_cast<const uint16_t*>(H), n_src, row_index, n_rows, c->d, c->stH, st) !=
+        cudaSuccess)
+      return JET_ERR_CUDA;
+  }
   PrepArgs pa;
   pa.n_rows = n_rows;
   pa.n_tok = n_tok;
   pa.V = c->V;
+  pa.row_index = row_index;
+  pa.n_src = n_src;
   pa.tok_row = tok_row;
   pa.tok_ids = tok_ids;
   pa.cand_offsets = cand_offsets;
@@ -343,7 +355,8 @@ int score_sets_enqueue(jet_ctx* c, const void* H, const void* W, int n_rows, con
     ProfScope ps(c, K_PREP, st);
     if (launch_prep(pa, st) != cudaSuccess) return JET_ERR_CUDA;
   }
-  const int rc = run_full_head(c, H, W, n_rows, sa.logp, o.lse, c->lse_row, st);
+  const int rc = run_full_head(c, row_index ? static_cast<const void*>(c->stH) : H, W, n_rows, sa.logp, o.lse,
+                               c->lse_row, st);
   if (rc != JET_OK) return rc;
   sa.zg = c->zg;            // logp = z - lse(row), formed by the set kernel
   sa.lse_row = c->lse_row;
@@ -653,6 +666,37 @@ int jet_sync_status(jet_ctx* c, void* stream) {
   if (!c) return JET_ERR_ARG;
   DeviceGuard g(c->device);
   if (!g.ok) return JET_ERR_CUDA;
+  return read_status(c, static_cast<cudaStream_t>(stream));
+}
+
+int jet_score_sets_gather_async(jet_ctx* c, const void* H_src, int n_src_rows, const int32_t* row_index,
+                                int n_rows, const void* W, const int32_t* tok_row, const int32_t* tok_ids,
+                                int n_tok, const int32_t* cand_offsets, int n_cand, const int32_t* set_offsets,
+                                const uint8_t* kind, int n_sets, float T, int mode, const int32_t* union_ids,
+                                int n_union, const jet_set_out* out, void* stream) {
+  const int rc = check_sets_args(c, H_src, W, n_rows, tok_row, tok_ids, n_tok, cand_offsets, n_cand, set_offsets,
+                                 kind, n_sets, T, mode, union_ids, n_union);
+  if (rc != JET_OK || n_tok == 0) return rc;
+  if (!row_index || n_src_rows < 1 || (reinterpret_cast<uintptr_t>(row_index) & 3u) != 0) return JET_ERR_ARG;
+  DeviceGuard g(c->device);
+  if (!g.ok) return JET_ERR_CUDA;
+  return score_sets_enqueue(c, H_src, W, n_rows, tok_row, tok_ids, n_tok, cand_offsets, n_cand, set_offsets, kind,
+                            n_sets, T, mode, union_ids, n_union, out, static_cast<cudaStream_t>(stream), row_index,
+                            n_src_rows);
+}
+
+int jet_score_sets_gather(jet_ctx* c, const void* H_src, int n_src_rows, const int32_t* row_index, int n_rows,
+                          const void* W, const int32_t* tok_row, const int32_t* tok_ids, int n_tok,
+                          const int32_t* cand_offsets, int n_cand, const int32_t* set_offsets, const uint8_t* kind,
+                          int n_sets, float T, int mode, const int32_t* union_ids, int n_union,
+                          const jet_set_out* out, void* stream) {
+  const int rc = jet_score_sets_gather_async(c, H_src, n_src_rows, row_index, n_rows, W, tok_row, tok_ids, n_tok,
+                                             cand_offsets, n_cand, set_offsets, kind, n_sets, T, mode, union_ids,
+                                             n_union, out, stream);
+  if (rc != JET_OK || n_tok == 0) {
+    if (rc == JET_ERR_CUDA && c) cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    return rc;
+  }
   return read_status(c, static_cast<cudaStream_t>(stream));
 }
 

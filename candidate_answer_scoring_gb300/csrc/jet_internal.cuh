@@ -138,6 +138,8 @@ __host__ __device__ __forceinline__ int plan_unit_of(const Plan& p, int m, int s
 // ---- launchers (each returns cudaGetLastError() of its launch) -------------
 struct PrepArgs {
   int n_rows, n_tok, V;
+  const int32_t* row_index = nullptr;   // gathered rows: each index must lie in [0, n_src); NULL: none
+  int n_src = 0;
   const int32_t* tok_row;   // NULL: token i is predicted by row i
   const int32_t* tok_ids;
   const int32_t* cand_offsets; int n_cand;   // NULL when no sets (jet_score_tokens)
@@ -148,6 +150,11 @@ struct PrepArgs {
   int* err;
 };
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t st);
+
+// Copy rows src[row_index[i]] (i < n_rows) to dst[i]; indices outside
+// [0, n_src) are skipped (the pre-pass reports them).  d % 8 == 0.
+cudaError_t launch_gather_rows(const uint16_t* src, int n_src, const int32_t* row_index, int n_rows, int d,
+                               uint16_t* dst, cudaStream_t st);
 
 // tmW's box must have HeadShape<a.plan.pair>::B_ROWS rows; tmH's box BM rows.
 cudaError_t launch_head(const CUtensorMap& tmH, const CUtensorMap& tmW, const HeadArgs& a,
@@ -168,6 +175,10 @@ cudaError_t launch_merge(const MergeArgs& a, cudaStream_t st);
 struct RestrictedArgs {
   int N, d, V, n_union, num_sms;
   const uint16_t* H; const uint16_t* W; const int32_t* union_ids;
+  // NULL: row r is H[r]; else H[row_index[r]] with indices checked against
+  // n_src (an index out of range is read as row 0 and reported by the set kernel)
+  const int32_t* row_index = nullptr;
+  int n_src = 0;
   float* zu;        // [N * n_union] logits over the union, or NULL (recomputed per token)
   float* lse_row;   // [N] log-sum-exp over the union
   float* lse;       // [N] caller's output or NULL

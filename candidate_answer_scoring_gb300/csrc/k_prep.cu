@@ -53,6 +53,13 @@ __global__ void __launch_bounds__(PREP_THREADS) prep_kernel(PrepArgs a) {
     if (!identity && j > 0 && a.tok_row[j - 1] > r) s_unsorted = 1;
   }
 
+  // gathered rows: every index within the source array
+  if (a.row_index)
+    for (int i = tid; i < a.n_rows; i += nth) {
+      const int idx = a.row_index[i];
+      if (idx < 0 || idx >= a.n_src) set_error(err, JET_ERR_TOKEN_RANGE, i);
+    }
+
   // candidate and set offsets (CSR), kind constraints
   if (a.cand_offsets) {
     if (tid == 0) {
@@ -172,7 +179,35 @@ __global__ void __launch_bounds__(PREP_THREADS) prep_kernel(PrepArgs a) {
   }
 }
 
+// Answer-position rows read in place from a larger source: one warp per row,
+// 16-byte vectors, grid-stride.  The head then streams the compact copy with
+// tiled TMA loads.  (Gathering inside the head's A-operand loads, four rows
+// per TMA gather, was measured on GB300 at about four times the head's time:
+// the A tile is fetched again for every vocabulary tile, and each 512-byte
+// gather costs the TMA unit about as much as a 16 KB tile.)
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* src, int n_src, const int32_t* row_index,
+                                                          int n_rows, int nvec, uint4* dst) {
+  pdl_wait();      // earlier work on the stream is complete before any access
+  pdl_trigger();   // the pre-pass may start; it waits for this grid before the head reads dst
+  const int lane = threadIdx.x & 31;
+  for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < n_rows; r += (gridDim.x * blockDim.x) >> 5) {
+    const int idx = row_index[r];
+    if (idx < 0 || idx >= n_src) continue;
+    const uint4* s = src + (size_t)idx * nvec;
+    uint4* o = dst + (size_t)r * nvec;
+    for (int k = lane; k < nvec; k += 32) o[k] = s[k];
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_gather_rows(const uint16_t* src, int n_src, const int32_t* row_index, int n_rows, int d,
+                               uint16_t* dst, cudaStream_t st) {
+  if (n_rows <= 0) return cudaSuccess;
+  const int blocks = (n_rows + 7) / 8 < 1184 ? (n_rows + 7) / 8 : 1184;   // 8 rows per block, at most 8 per SM
+  return launch_dependent(gather_rows_kernel, dim3(blocks), dim3(256), 0, st, reinterpret_cast<const uint4*>(src),
+                          n_src, row_index, n_rows, d / 8, reinterpret_cast<uint4*>(dst));
+}
 
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t st) {
   if (a.tok_row != nullptr && a.n_rows + 1 <= PREP_SMEM_ROWS)

@@ -92,6 +92,14 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// Row of H holding problem row r: r itself, or row_index[r] when gathering
+// (an index outside [0, n_src) reads row 0; the set kernel reports it).
+__device__ __forceinline__ int source_row(const RestrictedArgs& a, int r) {
+  if (a.row_index == nullptr) return r;
+  const int idx = a.row_index[r];
+  return (idx >= 0 && idx < a.n_src) ? idx : 0;
+}
+
 // Fragment mapping.  In an m16n8k16 MMA, lane (g = lane/4, c = lane%4) holds
 // A elements (rows g and g+8) and B elements (code g) at k slots {2c, 2c+1,
 // 2c+8, 2c+9}.  A dot product does not care which physical k feeds which slot
@@ -120,8 +128,8 @@ __global__ void __launch_bounds__(RT_THREADS, 1) restricted_head_kernel(const Re
   // results of rows past N are never written)
   const int nch = d / 32;                                    // 32-wide k chunks
   const int ch0 = warp * nch / RT_WARPS, ch1 = (warp + 1) * nch / RT_WARPS;
-  const uint4* hA = reinterpret_cast<const uint4*>(a.H + (size_t)min(r0 + g, a.N - 1) * d) + c;
-  const uint4* hB = reinterpret_cast<const uint4*>(a.H + (size_t)min(r0 + g + 8, a.N - 1) * d) + c;
+  const uint4* hA = reinterpret_cast<const uint4*>(a.H + (size_t)source_row(a, min(r0 + g, a.N - 1)) * d) + c;
+  const uint4* hB = reinterpret_cast<const uint4*>(a.H + (size_t)source_row(a, min(r0 + g + 8, a.N - 1)) * d) + c;
 
   for (int u0 = 0; u0 < U; u0 += RT_CODES) {
     const uint4* wr[4];
@@ -262,6 +270,11 @@ __global__ void __launch_bounds__(32 * RS_WARPS) restricted_sets_kernel(const Re
   const int U = ra.n_union;
   pdl_wait();
   pdl_trigger();
+  if (ra.row_index)   // gathered rows: every index within the source array
+    for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < ra.N; r += gridDim.x * blockDim.x) {
+      const int idx = ra.row_index[r];
+      if (idx < 0 || idx >= ra.n_src) set_error(err, JET_ERR_TOKEN_RANGE, r);
+    }
   if (blockIdx.x == 0 && wib == 0) {
     if (lane == 0) {
       if (sa.set_offsets[0] != 0 || sa.set_offsets[sa.n_sets] != a.n_cand) set_error(err, JET_ERR_OFFSETS, 0);
@@ -308,7 +321,7 @@ __global__ void __launch_bounds__(32 * RS_WARPS) restricted_sets_kernel(const Re
     for (int c = c0; c < c1; ++c) {
       const int t0 = sa.cand_offsets[c];
       const int t = sa.tok_ids[t0], r = a.tok_row[t0];
-      const float z = dot_row(reinterpret_cast<const uint4*>(ra.H) + (size_t)r * nvec,
+      const float z = dot_row(reinterpret_cast<const uint4*>(ra.H) + (size_t)source_row(ra, r) * nvec,
                               reinterpret_cast<const uint4*>(ra.W) + (size_t)t * nvec, nvec, lane);
       if (lane == 0) sa.logp[t0] = z - ra.lse_row[r];
     }

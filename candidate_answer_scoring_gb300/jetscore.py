@@ -70,6 +70,8 @@ def load() -> C.CDLL:
     sets_sig = [P, P, P, I, P, P, I, P, I, P, P, I, F, I, P, I, C.POINTER(_SetOut), P]
     for name in ("jet_score_sets", "jet_score_sets_async", "jet_score_sets_host"):
         getattr(lib, name).argtypes = sets_sig
+    for name in ("jet_score_sets_gather", "jet_score_sets_gather_async"):
+        getattr(lib, name).argtypes = [P, P, I, P, I, P, P, P, I, P, I, P, P, I, F, I, P, I, C.POINTER(_SetOut), P]
     lib.jet_sync_status.argtypes = [P, P]
     lib.jet_plan_info.argtypes = [P, I, C.POINTER(C.c_int)]
     lib.jet_profile_enable.argtypes = [P, I]
@@ -192,6 +194,33 @@ class JetScorer:
         rc = fn(*args, _stream(dev))
         if rc != JET_OK:
             raise JetError(rc, "jet_score_sets")
+        return out
+
+    def score_sets_gather(self, H_src, row_index, W, tok_row, tok_ids, cand_offsets, set_offsets, kind, T: float,
+                          mode: int = JET_MODE_FULL, union_ids=None,
+                          out: Optional[Dict[str, torch.Tensor]] = None, sync: bool = True) -> Dict[str, torch.Tensor]:
+        """score_sets with row i of the problem read in place as H_src[row_index[i]]
+        (e.g. the answer positions of a right-padded [B*L, d] backbone output)."""
+        dev = self.device
+        _check_dev(H_src, "H_src", dev, _BF16); _check_dev(W, "W", dev, _BF16)
+        for name, t in (("row_index", row_index), ("tok_row", tok_row), ("tok_ids", tok_ids),
+                        ("cand_offsets", cand_offsets), ("set_offsets", set_offsets)):
+            _check_dev(t, name, dev, (torch.int32,))
+        _check_dev(kind, "kind", dev, (torch.uint8,))
+        if union_ids is not None:
+            _check_dev(union_ids, "union_ids", dev, (torch.int32,))
+        n_rows = row_index.numel()
+        if out is None:
+            out = self.alloc_outputs(n_rows, tok_ids.numel(), cand_offsets.numel() - 1, set_offsets.numel() - 1)
+        so = _SetOut(*[_ptr(out.get(n)) for n in SET_OUTPUTS])
+        n_union = 0 if union_ids is None else union_ids.numel()
+        fn = self.lib.jet_score_sets_gather if sync else self.lib.jet_score_sets_gather_async
+        rc = fn(
+            self._h, _ptr(H_src), H_src.shape[0], _ptr(row_index), n_rows, _ptr(W), _ptr(tok_row), _ptr(tok_ids),
+            tok_ids.numel(), _ptr(cand_offsets), cand_offsets.numel() - 1, _ptr(set_offsets), _ptr(kind),
+            set_offsets.numel() - 1, C.c_float(T), int(mode), _ptr(union_ids), n_union, C.byref(so), _stream(dev))
+        if rc != JET_OK:
+            raise JetError(rc, "jet_score_sets_gather")
         return out
 
     KERNELS = ("prep", "head", "merge", "restricted", "sets")

@@ -146,6 +146,36 @@ int jet_score_sets(jet_ctx *ctx, const void *H_bf16, const void *W_bf16, int n_r
                    int n_union, const jet_set_out *out, void *cuda_stream);
 
 /*
+ * jet_score_sets_gather: jet_score_sets with the hidden rows read in place from
+ * a larger source array, such as a right-padded backbone output [B * L, d]
+ * whose scored rows sit at each sequence's answer (last valid) position
+ * (Gemma/MLX architecture page, "Backbone and precision": right padding and
+ * row-specific answer positions; PARALLEL_SCORING page, "Execution" step 4:
+ * scores use each row's last valid position).  Row i of the problem is
+ * H_src[row_index[i]].  Full mode copies the gathered rows once into the
+ * context's staging buffer (one warp per row) and streams them from there
+ * with tiled loads; restricted mode reads them in place.
+ *   H_src_bf16 [n_src_rows, d] bf16 (device, 16-byte aligned);
+ *   row_index [n_rows] int32 (device), each in
+ *   [0, n_src_rows); rows may repeat.  Every other argument is as in
+ *   jet_score_sets, with n_rows the number of gathered rows and tok_row
+ *   indexing them.
+ * Errors: as jet_score_sets; a row_index outside [0, n_src_rows) gives
+ * JET_ERR_TOKEN_RANGE.  Synchronous; jet_score_sets_gather_async returns
+ * after enqueueing, like jet_score_sets_async (status via jet_sync_status).
+ */
+int jet_score_sets_gather(jet_ctx *ctx, const void *H_src_bf16, int n_src_rows, const int32_t *row_index,
+                          int n_rows, const void *W_bf16, const int32_t *tok_row, const int32_t *tok_ids,
+                          int n_tok, const int32_t *cand_offsets, int n_cand, const int32_t *set_offsets,
+                          const uint8_t *kind, int n_sets, float T, int mode, const int32_t *union_ids,
+                          int n_union, const jet_set_out *out, void *cuda_stream);
+int jet_score_sets_gather_async(jet_ctx *ctx, const void *H_src_bf16, int n_src_rows, const int32_t *row_index,
+                                int n_rows, const void *W_bf16, const int32_t *tok_row, const int32_t *tok_ids,
+                                int n_tok, const int32_t *cand_offsets, int n_cand, const int32_t *set_offsets,
+                                const uint8_t *kind, int n_sets, float T, int mode, const int32_t *union_ids,
+                                int n_union, const jet_set_out *out, void *cuda_stream);
+
+/*
  * jet_score_sets_async: as jet_score_sets but returns after enqueueing (host
  * checks only).  The device status of the last enqueued call is returned by
  * jet_sync_status, which waits for `cuda_stream`.  For benchmarking and
