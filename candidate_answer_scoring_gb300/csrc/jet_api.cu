@@ -89,6 +89,7 @@ constexpr int UNITS_PER_SM_CAP = 64;   // bound on schedule units (partials work
 // logits in the set kernel instead.
 constexpr size_t ZU_FLOATS_PER_ROW = 128;
 constexpr size_t ZU_FLOATS_MIN = size_t(1) << 20;
+constexpr size_t IO_HEAD = 64;   // bytes of the error words at the front of the output block
 
 template <class T>
 cudaError_t dalloc(T** p, size_t n) {
@@ -119,8 +120,12 @@ struct jet_ctx {
   float *expd = nullptr, *conf = nullptr, *mass = nullptr;
   // device staging of host inputs (jet_score_sets_host)
   uint16_t* stH = nullptr;
-  int32_t *st_row = nullptr, *st_tok = nullptr, *st_co = nullptr, *st_so = nullptr, *st_union = nullptr;
-  uint8_t* st_kind = nullptr;
+  // jet_score_sets_host packs the small inputs into one pinned block (one
+  // copy in) and lays the requested outputs out behind the error word in one
+  // device block (one copy out, status included)
+  uint8_t *h_in = nullptr, *d_in = nullptr;     // pinned host / device, in_cap bytes
+  uint8_t *io_dev = nullptr, *h_out = nullptr;  // device / pinned host: [IO_HEAD error words][outputs]
+  size_t in_cap = 0, out_cap = 0;
   int* h_err = nullptr;   // pinned
   // row deduplication workspace
   unsigned long long *dd_hash = nullptr, *dd_keys = nullptr;
@@ -425,7 +430,10 @@ int jet_create(jet_ctx** out, int d, int V, int max_rows, int max_tokens, int de
   const size_t R = (size_t)max_rows, Tk = (size_t)max_tokens;
   cudaError_t e = cudaSuccess;
   auto A = [&](cudaError_t r) { if (e == cudaSuccess) e = r; };
-  A(dalloc(&c->err, ERR_WORDS));
+  c->out_cap = IO_HEAD + (8 * Tk + R) * 4 + 9 * 16;   // the nine outputs, each 16-byte aligned
+  c->in_cap = (4 * Tk + 2 + JET_MAX_UNION) * 4 + Tk + 6 * 16;   // rows, ids, two offset arrays, union, kind
+  A(dalloc(&c->io_dev, c->out_cap));
+  c->err = reinterpret_cast<int*>(c->io_dev);   // the error words head the output block
   A(dalloc(&c->row_ptr, R + 1));
   A(dalloc(&c->row_cur, R + 1));
   A(dalloc(&c->row_list, Tk));
@@ -447,12 +455,9 @@ int jet_create(jet_ctx** out, int d, int V, int max_rows, int max_tokens, int de
   A(dalloc(&c->conf, Tk));
   A(dalloc(&c->mass, Tk));
   A(dalloc(&c->stH, R * (size_t)d));
-  A(dalloc(&c->st_row, Tk));
-  A(dalloc(&c->st_tok, Tk));
-  A(dalloc(&c->st_co, Tk + 1));
-  A(dalloc(&c->st_so, Tk + 1));
-  A(dalloc(&c->st_kind, Tk));
-  A(dalloc(&c->st_union, (size_t)JET_MAX_UNION));
+  A(dalloc(&c->d_in, c->in_cap));
+  A(cudaMallocHost(reinterpret_cast<void**>(&c->h_in), c->in_cap));
+  A(cudaMallocHost(reinterpret_cast<void**>(&c->h_out), c->out_cap));
   c->dd_table = 1;
   while (c->dd_table < 2 * max_rows) c->dd_table <<= 1;
   A(dalloc(&c->dd_hash, R));
@@ -476,15 +481,17 @@ void jet_destroy(jet_ctx* c) {
   if (!c) return;
   DeviceGuard g(c->device);
   cudaDeviceSynchronize();
-  void* ptrs[] = {c->err, c->row_ptr, c->row_cur, c->row_list, c->iscratch, c->lse_row, c->umap, c->zu, c->zg, c->part, c->hash,
+  void* ptrs[] = {c->io_dev, c->row_ptr, c->row_cur, c->row_list, c->iscratch, c->lse_row, c->umap, c->zu, c->zg, c->part, c->hash,
                   c->lse, c->logp, c->s, c->q, c->qe, c->dec, c->expd, c->conf, c->mass, c->stH,
-                  c->st_row, c->st_tok, c->st_co, c->st_so, c->st_kind, c->st_union,
+                  c->d_in,
                   c->dd_hash, c->dd_keys, c->dd_vals, c->dd_rep, c->dd_rank};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   for (auto& v : c->ev)
     for (cudaEvent_t e : v) cudaEventDestroy(e);
   if (c->h_err) cudaFreeHost(c->h_err);
+  if (c->h_in) cudaFreeHost(c->h_in);
+  if (c->h_out) cudaFreeHost(c->h_out);
   if (c->h_fit) cudaFreeHost(c->h_fit);
   if (c->fit_res) cudaFree(c->fit_res);
   delete c;
@@ -761,58 +768,74 @@ int jet_score_sets_host(jet_ctx* c, const void* H, const void* W, int n_rows, co
   DeviceGuard g(c->device);
   if (!g.ok) return JET_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaSuccess;
-  auto H2D = [&](void* dst, const void* src, size_t bytes) {
-    if (e == cudaSuccess && bytes) e = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, st);
+  // inputs: H straight from the caller, the index arrays packed into one
+  // pinned block (16-byte aligned pieces) and copied in once
+  size_t in_off = 0;
+  auto pack = [&](const void* src, size_t bytes) -> const void* {
+    uint8_t* dst = c->d_in + in_off;
+    std::memcpy(c->h_in + in_off, src, bytes);
+    in_off += (bytes + 15) & ~size_t(15);
+    return dst;
   };
-  H2D(c->stH, H, (size_t)n_rows * c->d * 2);
-  H2D(c->st_row, tok_row, (size_t)n_tok * 4);
-  H2D(c->st_tok, tok_ids, (size_t)n_tok * 4);
-  H2D(c->st_co, cand_offsets, (size_t)(n_cand + 1) * 4);
-  H2D(c->st_so, set_offsets, (size_t)(n_sets + 1) * 4);
-  H2D(c->st_kind, kind, (size_t)n_sets);
-  const int32_t* dev_union = nullptr;
-  if (mode == JET_MODE_RESTRICTED) {
-    H2D(c->st_union, union_ids, (size_t)n_union * 4);
-    dev_union = c->st_union;
-  }
-  if (e != cudaSuccess) return JET_ERR_CUDA;
+  const int32_t* d_row = static_cast<const int32_t*>(pack(tok_row, (size_t)n_tok * 4));
+  const int32_t* d_tok = static_cast<const int32_t*>(pack(tok_ids, (size_t)n_tok * 4));
+  const int32_t* d_co = static_cast<const int32_t*>(pack(cand_offsets, (size_t)(n_cand + 1) * 4));
+  const int32_t* d_so = static_cast<const int32_t*>(pack(set_offsets, (size_t)(n_sets + 1) * 4));
+  const uint8_t* d_kind = static_cast<const uint8_t*>(pack(kind, (size_t)n_sets));
+  const int32_t* d_union =
+      mode == JET_MODE_RESTRICTED ? static_cast<const int32_t*>(pack(union_ids, (size_t)n_union * 4)) : nullptr;
+  if (cudaMemcpyAsync(c->stH, H, (size_t)n_rows * c->d * 2, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(c->d_in, c->h_in, in_off, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return JET_ERR_CUDA;
+
+  // outputs: the requested ones behind the error words, in one device block
+  jet_set_out h;
+  std::memset(&h, 0, sizeof h);
+  if (out_host) h = *out_host;
   jet_set_out dev;
-  dev.logp = c->logp;
-  dev.lse = c->lse;
-  dev.s = c->s;
-  dev.q = c->q;
-  dev.q_equiv = c->qe;
-  dev.decision = c->dec;
-  dev.expected = c->expd;
-  dev.confidence = c->conf;
-  dev.mass = c->mass;
-  rc = score_sets_enqueue(c, c->stH, W, n_rows, c->st_row, c->st_tok, n_tok, c->st_co, n_cand, c->st_so,
-                          c->st_kind, n_sets, T, mode, dev_union, n_union, &dev, st);
+  std::memset(&dev, 0, sizeof dev);
+  size_t out_off = IO_HEAD;
+  auto place = [&](void* host_ptr, size_t bytes) -> uint8_t* {
+    if (!host_ptr) return nullptr;
+    uint8_t* p = c->io_dev + out_off;
+    out_off += (bytes + 15) & ~size_t(15);
+    return p;
+  };
+  dev.logp = reinterpret_cast<float*>(place(h.logp, (size_t)n_tok * 4));
+  dev.lse = reinterpret_cast<float*>(place(h.lse, (size_t)n_rows * 4));
+  dev.s = reinterpret_cast<float*>(place(h.s, (size_t)n_cand * 4));
+  dev.q = reinterpret_cast<float*>(place(h.q, (size_t)n_cand * 4));
+  dev.q_equiv = reinterpret_cast<float*>(place(h.q_equiv, (size_t)n_cand * 4));
+  dev.decision = reinterpret_cast<int32_t*>(place(h.decision, (size_t)n_sets * 4));
+  dev.expected = reinterpret_cast<float*>(place(h.expected, (size_t)n_sets * 4));
+  dev.confidence = reinterpret_cast<float*>(place(h.confidence, (size_t)n_sets * 4));
+  dev.mass = reinterpret_cast<float*>(place(h.mass, (size_t)n_sets * 4));
+  rc = score_sets_enqueue(c, c->stH, W, n_rows, d_row, d_tok, n_tok, d_co, n_cand, d_so, d_kind, n_sets, T, mode,
+                          d_union, n_union, &dev, st);
   if (rc != JET_OK) {
     cudaStreamSynchronize(st);
     return rc;
   }
-  jet_set_out h;
-  std::memset(&h, 0, sizeof h);
-  if (out_host) h = *out_host;
-  auto D2H = [&](void* dst, const void* src, size_t bytes) {
-    if (e == cudaSuccess && dst && bytes) e = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToHost, st);
-  };
-  D2H(h.logp, c->logp, (size_t)n_tok * 4);
-  D2H(h.lse, c->lse, (size_t)n_rows * 4);
-  D2H(h.s, c->s, (size_t)n_cand * 4);
-  D2H(h.q, c->q, (size_t)n_cand * 4);
-  D2H(h.q_equiv, c->qe, (size_t)n_cand * 4);
-  D2H(h.decision, c->dec, (size_t)n_sets * 4);
-  D2H(h.expected, c->expd, (size_t)n_sets * 4);
-  D2H(h.confidence, c->conf, (size_t)n_sets * 4);
-  D2H(h.mass, c->mass, (size_t)n_sets * 4);
-  if (e != cudaSuccess) {
+  // one copy back: error words and every requested output
+  if (cudaMemcpyAsync(c->h_out, c->io_dev, out_off, cudaMemcpyDeviceToHost, st) != cudaSuccess) {
     cudaStreamSynchronize(st);
     return JET_ERR_CUDA;
   }
-  return read_status(c, st);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return JET_ERR_CUDA;
+  const int status = reinterpret_cast<const int*>(c->h_out)[0];
+  auto unpack = [&](void* host_ptr, const void* dev_ptr, size_t bytes) {
+    if (host_ptr) std::memcpy(host_ptr, c->h_out + (static_cast<const uint8_t*>(dev_ptr) - c->io_dev), bytes);
+  };
+  unpack(h.logp, dev.logp, (size_t)n_tok * 4);
+  unpack(h.lse, dev.lse, (size_t)n_rows * 4);
+  unpack(h.s, dev.s, (size_t)n_cand * 4);
+  unpack(h.q, dev.q, (size_t)n_cand * 4);
+  unpack(h.q_equiv, dev.q_equiv, (size_t)n_cand * 4);
+  unpack(h.decision, dev.decision, (size_t)n_sets * 4);
+  unpack(h.expected, dev.expected, (size_t)n_sets * 4);
+  unpack(h.confidence, dev.confidence, (size_t)n_sets * 4);
+  unpack(h.mass, dev.mass, (size_t)n_sets * 4);
+  return status;
 }
 
 }  // extern "C"

@@ -217,6 +217,35 @@ def test_host_entry_matches_device_entry(jet):
         assert np.array_equal(host[k].numpy().view(np.uint32), dev[k].view(np.uint32)), k
 
 
+def test_host_entry_restricted_subset_and_errors(jet):
+    """The host entry packs the index arrays into one copy in and the requested
+    outputs (behind the status words) into one copy out: restricted mode, a
+    subset of outputs, and an error status all come back through it."""
+    import candidate_answer_scoring_gb300 as j
+    base = wk.binary_batch(n_questions=48, random_pairs=True, d=128, V=2000)
+    wl = wk.binary_restricted(base=base)
+    sc = jet.JetScorer(wl.d, wl.V, wl.N, wl.n_tok)
+    x = to_dev(wl)
+    dev = run_gpu(jet, wl, sc, x)
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    args = [pin(wl.H.view(np.int16)).view(torch.bfloat16), x["W"], pin(wl.tok_row), pin(wl.tok_ids),
+            pin(wl.cand_offsets), pin(wl.set_offsets), pin(wl.kind), wl.T, wl.mode, pin(wl.union_ids)]
+    want = {"q": torch.full((wl.n_cand,), -7.0), "decision": torch.full((wl.n_sets,), -7, dtype=torch.int32),
+            "mass": torch.full((wl.n_sets,), -7.0)}
+    host = sc.score_sets_host(*args, out=want)
+    for k in want:
+        assert np.array_equal(host[k].numpy().view(np.uint32), dev[k].view(np.uint32)), k
+    bad = wl.tok_ids.copy()
+    bad[5] = wl.V
+    args[3] = pin(bad)
+    with pytest.raises(j.JetError) as e:
+        sc.score_sets_host(*args, out=want)
+    assert e.value.status == -2
+    args[3] = pin(wl.tok_ids)
+    host = sc.score_sets_host(*args)                                      # the context still works
+    compare(wl, {k: v.numpy() for k, v in host.items()}, oracle.score_workload(wl))
+
+
 def test_outputs_leave_guard_bands_untouched(jet):
     wl = wk.custom(64, 900, 15, K=(2, 6), length=(1, 4), seed=4)
     sc = jet.JetScorer(wl.d, wl.V, wl.N, wl.n_tok)
