@@ -1,6 +1,8 @@
 // C ABI of libjetscore: context and workspace, host-side argument checks, the
-// vocabulary-split schedule, TMA tensor maps, and the launch sequence
-//   pre-pass -> head (full vocabulary) or restricted head -> merge -> set rules.
+// vocabulary-split schedule, TMA tensor maps, and the launch sequences
+//   full vocabulary:  [row gather ->] pre-pass -> head -> merge -> set rules
+//   restricted union: restricted head -> validation + set rules
+// (each launch a programmatic dependent of the previous one).
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
