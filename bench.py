@@ -134,6 +134,22 @@ def dist_setup():
     return world, rank, local
 
 
+def max_over_ranks(x, world, device):
+    """The largest value of x over the ranks (x itself with one rank): every
+    rank's timed region counts, the slowest one sets the job's time."""
+    if world <= 1:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_step, steps, world, ms):
+    """Whole-job tokens/s: every replica scores tokens_per_step each step."""
+    return world * tokens_per_step * steps / (ms / 1e3)
+
+
 def make_workload(name, rank=0):
     import workloads as wk
     gen = getattr(wk, WORKLOADS[name][0])
@@ -350,12 +366,9 @@ def gpu_arm(args, world, rank, local):
         rc = sc.sync_status()
         if rc != 0:
             raise RuntimeError(f"device status {rc} ({jet.status_string(rc)}) in the timed region")
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(ms, world, dev)
     tokens_per_step = steps_wl[0].n_tok
-    value = world * tokens_per_step * K / (ms / 1e3)
+    value = job_throughput(tokens_per_step, K, world, ms)
     ms_step = ms / K
 
     # kernel roofline: the full-vocabulary head
@@ -437,11 +450,8 @@ def gpu_arm(args, world, rank, local):
                                        out=hi["out"])
             torch.cuda.synchronize(dev)
             el = time.perf_counter() - t0
-        if world > 1:
-            tt = torch.tensor([el], device=dev)
-            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-            el = float(tt.item())
-        line["e2e"] = {"value": world * tokens_per_step * Ke / el, "unit": UNIT, "h2d_bytes_per_step": h2d,
+        el = max_over_ranks(el, world, dev)
+        line["e2e"] = {"value": job_throughput(tokens_per_step, Ke, world, el * 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                        "d2h_bytes_per_step": d2h, "steps": Ke, "ms_per_step": 1e3 * el / Ke,
                        "note": "jet_score_sets_host per mode: pinned host inputs -> device -> host results; "
                                "W resident on the device like any model weight"}
@@ -546,7 +556,7 @@ def op_arm(args):
     return 0
 
 
-def main():
+def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
@@ -561,7 +571,11 @@ def main():
                     help="score each distinct hidden row once (jet_dedup_rows before every step)")
     ap.add_argument("--op", default=None, choices=["dedup", "fit_temperature", "layer_sensitivity"],
                     help="time one of the widened ops instead of the scoring path")
-    args = ap.parse_args()
+    return ap.parse_args(argv)
+
+
+def main():
+    args = parse_args()
     world, rank, local = dist_setup()
     if args.op is not None:
         return op_arm(args)
