@@ -195,6 +195,28 @@ def test_edge_cases(jet):
     compare(wl, gpu, oracle.score_workload(wl))
 
 
+@pytest.mark.parametrize("case", ["vocab-below-one-tile", "widest-rows", "single-code-union"])
+def test_shape_extremes(jet, case):
+    """A vocabulary smaller than one 256-column tile (every column ragged), the
+    widest rows the library accepts (d = 16384: 256 k-blocks per tile) through
+    the full-vocabulary head with both head variants' row counts, and a
+    restricted union of one code (lse_U = z, so logp = 0 and q = 1)."""
+    if case == "vocab-below-one-tile":
+        wls = [wk.custom(64, 100, 6, K=(1, 5), length=(1, 3), seed=91)]
+    elif case == "widest-rows":
+        wls = [wk.custom(16384, 700, 4, K=(2, 4), length=(1, 2), seed=92),      # N <= 128: one-CTA head
+               wk.binary_batch(150, random_pairs=True, d=16384, V=600)]          # N > 128: paired head
+    else:
+        base = wk.custom(64, 400, 5, K=(1, 1), length=(1, 1), kinds=(0,), seed=93)
+        wls = [base.with_mode(wk.MODE_RESTRICTED, 1.0, np.unique(base.tok_ids)[:1])]
+        wls[0].tok_ids[:] = wls[0].union_ids[0]
+    for wl in wls:
+        gpu = run_gpu(jet, wl)
+        compare(wl, gpu, oracle.score_workload(wl))
+        if case == "single-code-union":
+            assert np.all(gpu["logp"] == 0.0) and np.all(gpu["q"] == 1.0)
+
+
 def test_repeat_calls_are_bitwise_deterministic(jet):
     wl = wk.custom(128, 2500, 30, K=(2, 8), length=(1, 5), seed=21)
     sc = jet.JetScorer(wl.d, wl.V, wl.N, wl.n_tok)
