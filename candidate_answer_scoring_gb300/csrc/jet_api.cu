@@ -104,7 +104,7 @@ struct jet_ctx {
   int device = 0, d = 0, V = 0, max_rows = 0, max_tokens = 0, num_sms = 0, units_cap = 0;
   EncodeTiledFn encode = nullptr;
   // device workspace
-  int* err = nullptr;
+  int* err = nullptr;        // error words: the head of io_dev (below)
   int* row_ptr = nullptr;
   int* row_cur = nullptr;
   int2* row_list = nullptr;
@@ -120,7 +120,8 @@ struct jet_ctx {
   float *lse = nullptr, *logp = nullptr, *s = nullptr, *q = nullptr, *qe = nullptr;
   int32_t* dec = nullptr;
   float *expd = nullptr, *conf = nullptr, *mass = nullptr;
-  // device staging of host inputs (jet_score_sets_host)
+  // [max_rows, d] staging copy of H: host inputs (jet_score_sets_host) and
+  // gathered rows (jet_score_sets_gather)
   uint16_t* stH = nullptr;
   // jet_score_sets_host packs the small inputs into one pinned block (one
   // copy in) and lays the requested outputs out behind the error word in one
