@@ -66,17 +66,52 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeArgs a) {
   else a.logp[r] = a.zg[r] - lse;
 }
 
+// One warp per set.  The set's index arrays are the caller's inputs, which
+// nothing in this call writes and which the pre-pass has already validated
+// (it completed before the head did, and the head completed before this grid
+// was launched), so they are read while the merge still runs; only the
+// gathered logits and row lse wait for it.  Sets of up to 32 single-token
+// candidates take the whole chain that way (lane i = candidate i); others
+// apply the chain rule after the wait.
 __global__ void __launch_bounds__(256) sets_kernel(const SetArgs a) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
+  const bool live = warp < a.n_sets && *(volatile const int*)a.err == 0;
+  int c0 = 0, c1 = 0, t0 = 0, row = 0, tok = 0;
+  bool single = false;
+  if (live) {
+    c0 = a.set_offsets[warp];
+    c1 = a.set_offsets[warp + 1];
+    if (c1 - c0 <= 32 && lane < c1 - c0) {
+      t0 = a.cand_offsets[c0 + lane];
+      single = a.cand_offsets[c0 + lane + 1] - t0 == 1;
+      if (single) {
+        row = a.tok_row[t0];
+        tok = a.tok_ids[t0];
+      }
+    }
+  }
   pdl_wait();
   pdl_trigger();   // the next call's first kernel may be scheduled; it waits for this grid
-  if (warp >= a.n_sets) return;
-  // the set's bounds are in range whatever the pre-pass found; they are
-  // loaded alongside the error word and used only once it reads clean
-  const int c0 = a.set_offsets[warp], c1 = a.set_offsets[warp + 1];
-  if (*(volatile const int*)a.err != 0) return;
-  set_rules_warp(a, warp, lane, c0, c1);
+  if (!live || *(volatile const int*)a.err != 0) return;
+  const int K = c1 - c0;
+  if (K > 32) {
+    set_rules_warp(a, warp, lane, c0, c1);
+    return;
+  }
+  float sc[1] = {-INFINITY};
+  unsigned long long h[1] = {0};
+  if (lane < K) {
+    if (single) {
+      const float l = a.zg[t0] - a.lse_row[row];
+      a.logp[t0] = l;
+      sc[0] = 0.f + l;   // the chain rule over one token
+      h[0] = single_token_hash(tok);
+    } else {
+      sc[0] = chain_sum(a, c0 + lane, h[0]);
+    }
+  }
+  set_rules_core<1>(a, warp, lane, c0, K, 1.0f / a.T, sc, h);
 }
 
 }  // namespace

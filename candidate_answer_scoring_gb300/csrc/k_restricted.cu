@@ -132,6 +132,8 @@ __global__ void __launch_bounds__(RT_THREADS, 1) restricted_head_kernel(const Re
   const uint4* hB = reinterpret_cast<const uint4*>(a.H + (size_t)source_row(a, min(r0 + g + 8, a.N - 1)) * d) + c;
 
   for (int u0 = 0; u0 < U; u0 += RT_CODES) {
+    // this lane's code for the reduction below, loaded with the operands
+    const int t_lane = u0 + lane < U ? a.union_ids[u0 + lane] : -1;
     const uint4* wr[4];
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) {
@@ -185,8 +187,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1) restricted_head_kernel(const Re
       for (int w = 0; w < RT_WARPS; ++w) z += sAcc[w][row][lane];
       bool valid = u < U;
       if (valid) {
-        const int t = a.union_ids[u];
-        if (!(t >= 0 && t < a.V)) z = __int_as_float(0x7fc00000);   // reported by the set kernel
+        if (!(t_lane >= 0 && t_lane < a.V)) z = __int_as_float(0x7fc00000);   // reported by the set kernel
         if (a.zu && r < a.N) a.zu[(size_t)r * U + u] = z;
       }
       float m = valid ? z : -INFINITY;
@@ -268,6 +269,36 @@ __global__ void __launch_bounds__(32 * RS_WARPS) restricted_sets_kernel(const Re
   const RestrictedArgs& ra = a.r;
   int* err = ra.err;
   const int U = ra.n_union;
+
+  // Before the restricted head finishes: the caller's index arrays (nothing in
+  // this call writes them, and the head started only after everything earlier
+  // on the stream had finished), checked as they are followed.  Errors are
+  // held in registers and recorded after the wait (the head zeroes the error
+  // word first).
+  const bool live = k < sa.n_sets;
+  int c0 = 0, c1 = 0, kd = 0, set_code = 0;
+  int cand_code = 0, cand_at = 0, t0 = 0, tok = 0, row = 0;
+  if (live) {
+    c0 = sa.set_offsets[k];
+    c1 = sa.set_offsets[k + 1];
+    kd = a.kind[k];
+    const int K = c1 - c0;
+    if (!(c0 >= 0 && c0 < c1 && c1 <= a.n_cand)) set_code = JET_ERR_OFFSETS;
+    else if (kd > JET_KIND_ORDINAL) set_code = JET_ERR_ARG;
+    else if ((kd == JET_KIND_BINARY && K != 2) || (kd == JET_KIND_ORDINAL && K < 2)) set_code = JET_ERR_OFFSETS;
+    if (set_code == 0 && ra.zu && K <= 32 && lane < K) {
+      const int c = c0 + lane;
+      t0 = sa.cand_offsets[c];
+      const int t1 = sa.cand_offsets[c + 1];
+      if (!(t0 >= 0 && t0 < t1 && t1 <= a.n_tok)) { cand_code = JET_ERR_OFFSETS; cand_at = c; }
+      else if (t1 - t0 != 1) { cand_code = JET_ERR_MODE; cand_at = c; }
+      else {
+        tok = sa.tok_ids[t0];
+        row = a.tok_row[t0];
+        if (tok < 0 || tok >= ra.V || row < 0 || row >= ra.N) { cand_code = JET_ERR_TOKEN_RANGE; cand_at = t0; }
+      }
+    }
+  }
   pdl_wait();
   pdl_trigger();
   if (ra.row_index)   // gathered rows: every index within the source array
@@ -286,24 +317,49 @@ __global__ void __launch_bounds__(32 * RS_WARPS) restricted_sets_kernel(const Re
       else if (ra.umap[t] != u) set_error(err, JET_ERR_NOT_IN_UNION, u);   // a repeated id keeps one position
     }
   }
-  if (k >= sa.n_sets) return;
-
+  if (!live) return;
   // the set's own offsets and kind (consecutive sets share a boundary, so
   // with both ends checked above the sets tile [0, n_cand) exactly)
-  const int c0 = sa.set_offsets[k], c1 = sa.set_offsets[k + 1];
-  const int kd = a.kind[k];
-  if (!(c0 >= 0 && c0 < c1 && c1 <= a.n_cand)) {
-    if (lane == 0) set_error(err, JET_ERR_OFFSETS, k);
+  if (set_code != 0) {
+    if (lane == 0) set_error(err, set_code, k);
     return;
   }
   const int K = c1 - c0;
-  if (kd > JET_KIND_ORDINAL || (kd == JET_KIND_BINARY && K != 2) || (kd == JET_KIND_ORDINAL && K < 2)) {
-    if (lane == 0) set_error(err, kd > JET_KIND_ORDINAL ? JET_ERR_ARG : JET_ERR_OFFSETS, k);
+  if (ra.zu && K <= 32) {   // candidates followed before the wait: the union lookup remains
+    float sc[1] = {-INFINITY};
+    unsigned long long h[1] = {0};
+    bool bad = false;
+    if (lane < K) {
+      if (cand_code != 0) {
+        set_error(err, cand_code, cand_at);
+        bad = true;
+      } else {
+        const int pos = ra.umap[tok];
+        const float lse = ra.lse_row[row];
+        if (pos < 0 || pos >= U) {
+          set_error(err, JET_ERR_NOT_IN_UNION, t0);
+          bad = true;
+        } else {
+          const int uid = ra.union_ids[pos];
+          const float z = ra.zu[(size_t)row * U + pos];
+          if (uid != tok) {   // a stale map entry
+            set_error(err, JET_ERR_NOT_IN_UNION, t0);
+            bad = true;
+          } else {
+            const float lp = z - lse;
+            sa.logp[t0] = lp;
+            sc[0] = 0.f + lp;   // the chain rule over one token
+            h[0] = single_token_hash(tok);
+          }
+        }
+      }
+    }
+    if (__any_sync(0xffffffffu, bad)) return;
+    set_rules_core<1>(sa, k, lane, c0, K, 1.0f / sa.T, sc, h);
     return;
   }
   if (ra.zu && K <= 128) {
-    if (K <= 32) restricted_set_regs<1>(a, k, lane, c0, K);
-    else if (K <= 64) restricted_set_regs<2>(a, k, lane, c0, K);
+    if (K <= 64) restricted_set_regs<2>(a, k, lane, c0, K);
     else restricted_set_regs<4>(a, k, lane, c0, K);
     return;
   }
