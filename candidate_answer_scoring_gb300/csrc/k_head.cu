@@ -32,6 +32,7 @@
 //
 // Every mbarrier wait is bounded: on timeout the kernel records
 // JET_ERR_TIMEOUT, drains its own copies and MMAs, frees TMEM and returns.
+#include <atomic>
 #include <climits>
 
 #include "jet_internal.cuh"
@@ -512,12 +513,17 @@ __global__ void __launch_bounds__(HEAD_THREADS, 1)
 
 template <bool PAIR>
 cudaError_t launch_variant(const CUtensorMap& tmH, const CUtensorMap& tmW, const HeadArgs& a, cudaStream_t st) {
-  static bool configured = false;   // per process; the attribute is per function
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(head_lse_gather_kernel<PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         HeadShape<PAIR>::SMEM_BYTES);
+  // the shared-memory attribute belongs to the function on each device
+  static std::atomic<unsigned long long> configured{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+  if (bit == 0 || (configured.load() & bit) == 0) {
+    e = cudaFuncSetAttribute(head_lse_gather_kernel<PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             HeadShape<PAIR>::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured.fetch_or(bit);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.plan.grid);
