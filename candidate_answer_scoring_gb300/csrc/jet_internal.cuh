@@ -96,6 +96,7 @@ struct HeadArgs {
   float2* part;         // per (unit, CTA of the pair, column half, row): (max, sum exp(z - max))
   int* err;
   int pf_kblocks;       // L2 prefetch distance for W, in k-blocks of the CTA's stream (0: off)
+  int w_tiled = 0;      // tmW is the 4-D map of a tiled W (jet_tile_weights)
 };
 
 // Host: schedule for N rows on G SMs; units * (1 + pair) <= units_cap.
@@ -151,6 +152,9 @@ struct PrepArgs {
 };
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t st);
 
+// Tiled copy of W (layout stated in jetscore.h, "Tiled weights").
+cudaError_t launch_tile_weights(const uint16_t* W, int V, int d, uint16_t* W_tiled, cudaStream_t st);
+
 // Copy rows src[row_index[i]] (i < n_rows) to dst[i]; indices outside
 // [0, n_src) are skipped (the pre-pass reports them).  d % 8 == 0.
 cudaError_t launch_gather_rows(const uint16_t* src, int n_src, const int32_t* row_index, int n_rows, int d,
@@ -179,6 +183,7 @@ struct RestrictedArgs {
   // n_src (an index out of range is read as row 0 and reported by the set kernel)
   const int32_t* row_index = nullptr;
   int n_src = 0;
+  int w_tiled = 0;  // W in the tiled layout (jet_tile_weights)
   float* zu;        // [N * n_union] logits over the union, or NULL (recomputed per token)
   float* lse_row;   // [N] log-sum-exp over the union
   float* lse;       // [N] caller's output or NULL

@@ -82,6 +82,26 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m
       : "memory");
 }
 
+// Tiled W (4-D map over [tiles][k-blocks][128 rows][64]): the box at
+// (0, 0, kb, tile) is the same 128- or 256-row slice as the 2-D box at
+// (64 kb, 128 tile) of row-major W, one contiguous 16 KB read per 128 rows.
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int kb, int tile, uint64_t* bar,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %3, %4, %5}], [%2], %6;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(0), "r"(kb), "r"(tile), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_4d_pair(void* dst, const CUtensorMap* map, int kb, int tile, uint32_t bar,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %3, %4, %5}], [%2], %6;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(0), "r"(kb), "r"(tile), "l"(policy)
+      : "memory");
+}
+
 // Bring a tile into L2 ahead of its TMA load (no shared-memory destination).
 __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x, int y) {
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
@@ -338,13 +358,15 @@ __global__ void __launch_bounds__(HEAD_THREADS, 1)
               if (issuer) mbar_arrive_expect_tx(&full[stage], 2 * SH::STAGE_BYTES);   // both CTAs' halves
               const uint32_t bar = cluster_addr(&full[stage], 0);
               tma_load_2d_pair(sA + stage * SH::A_BYTES, &tmH, kb * BK, a_row, bar, pol_h);
-              tma_load_2d_pair(sB + stage * SH::B_BYTES, &tmW, kb * BK, b_row, bar, pol_w);
+              if (a.w_tiled) tma_load_4d_pair(sB + stage * SH::B_BYTES, &tmW, kb, b_row >> 7, bar, pol_w);
+              else tma_load_2d_pair(sB + stage * SH::B_BYTES, &tmW, kb * BK, b_row, bar, pol_w);
             } else {
               mbar_arrive_expect_tx(&full[stage], SH::STAGE_BYTES);
               tma_load_2d(sA + stage * SH::A_BYTES, &tmH, kb * BK, a_row, &full[stage], pol_h);
-              tma_load_2d(sB + stage * SH::B_BYTES, &tmW, kb * BK, b_row, &full[stage], pol_w);
+              if (a.w_tiled) tma_load_4d(sB + stage * SH::B_BYTES, &tmW, kb, b_row >> 7, &full[stage], pol_w);
+              else tma_load_2d(sB + stage * SH::B_BYTES, &tmW, kb * BK, b_row, &full[stage], pol_w);
             }
-            if (a.pf_kblocks > 0) {   // optional: more W bytes in flight than the ring holds
+            if (a.pf_kblocks > 0 && !a.w_tiled) {   // optional: more W bytes in flight than the ring holds
               const int ip = (vt - vt0) * kblocks + kb + a.pf_kblocks;
               const int vtp = vt0 + ip / kblocks;
               if (vtp < vt1) tma_prefetch_l2_2d(&tmW, (ip % kblocks) * BK, vtp * BN + (int)rank * SH::B_ROWS);

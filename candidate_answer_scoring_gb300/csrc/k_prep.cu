@@ -199,7 +199,33 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* src, int 
   }
 }
 
+// Tiled copy of W: output vector o (8 bf16) of tile T, k-block kb, row r,
+// vector j8 holds W[128 T + r][64 kb + 8 j8 .. +8], zero past row V.
+__global__ void __launch_bounds__(256) tile_weights_kernel(const uint4* W, int V, int d, uint4* out,
+                                                           long long n_vec) {
+  const int kbs = d / 64;
+  const int nvec_row = d / 8;
+  for (long long o = blockIdx.x * (long long)blockDim.x + threadIdx.x; o < n_vec;
+       o += (long long)gridDim.x * blockDim.x) {
+    const int j8 = (int)(o & 7);
+    const int r = (int)((o >> 3) & 127);
+    const long long tk = o >> 10;               // tile * kbs + kb
+    const int kb = (int)(tk % kbs);
+    const long long row = (tk / kbs) * 128 + r;
+    out[o] = row < V ? W[row * nvec_row + kb * 8 + j8] : make_uint4(0, 0, 0, 0);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_tile_weights(const uint16_t* W, int V, int d, uint16_t* W_tiled, cudaStream_t st) {
+  const long long n_vec = (long long)((V + 127) / 128) * 128 * (d / 8);
+  const long long want = (n_vec + 255) / 256;
+  const int blocks = (int)(want < 4096 ? want : 4096);
+  tile_weights_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const uint4*>(W), V, d,
+                                              reinterpret_cast<uint4*>(W_tiled), n_vec);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_gather_rows(const uint16_t* src, int n_src, const int32_t* row_index, int n_rows, int d,
                                uint16_t* dst, cudaStream_t st) {

@@ -58,9 +58,21 @@ __device__ __forceinline__ float dot_bf16x8(uint4 h, uint4 w, float acc) {
   return acc;
 }
 
+// Index of 16-byte vector j (elements 8j .. 8j+7) of W's row t, row-major or
+// tiled ([ceil(V/128)][d/64][128][64]: vector j of row t lies in k-block j/8
+// of tile t/128).  wbase = w_row_base(t).
+__device__ __forceinline__ size_t w_row_base(int t, int d, bool tiled) {
+  return tiled ? ((size_t)(t >> 7) * (d / 64) * 128 + (t & 127)) * 8 : (size_t)t * (d / 8);
+}
+__device__ __forceinline__ size_t w_vec(size_t wbase, int j, bool tiled) {
+  return tiled ? wbase + (size_t)(j >> 3) * 1024 + (j & 7) : wbase + j;
+}
+
 // h . w over nvec 16-byte bf16 vectors by one warp (lane l takes vectors l,
 // l+32, ...; a fixed butterfly combines the lanes; every lane gets the sum).
-__device__ __forceinline__ float dot_row(const uint4* h, const uint4* w, int nvec, int lane) {
+// w is row t of W: vector k at Wv[w_vec(wbase, k, tiled)].
+__device__ __forceinline__ float dot_row(const uint4* h, const uint4* Wv, size_t wbase, bool tiled, int nvec,
+                                         int lane) {
   float acc = 0.f;
   for (int k0 = lane; k0 < nvec; k0 += 32 * DR_BATCH) {
     uint4 hv[DR_BATCH / 2], wv[DR_BATCH / 2];
@@ -69,7 +81,7 @@ __device__ __forceinline__ float dot_row(const uint4* h, const uint4* w, int nve
 #pragma unroll
       for (int i = 0; i < DR_BATCH / 2; ++i) {
         const int k = kb + 32 * i;
-        if (k < nvec) { hv[i] = h[k]; wv[i] = w[k]; }
+        if (k < nvec) { hv[i] = h[k]; wv[i] = Wv[w_vec(wbase, k, tiled)]; }
       }
 #pragma unroll
       for (int i = 0; i < DR_BATCH / 2; ++i)
@@ -134,12 +146,14 @@ __global__ void __launch_bounds__(RT_THREADS, 1) restricted_head_kernel(const Re
   for (int u0 = 0; u0 < U; u0 += RT_CODES) {
     // this lane's code for the reduction below, loaded with the operands
     const int t_lane = u0 + lane < U ? a.union_ids[u0 + lane] : -1;
-    const uint4* wr[4];
+    const uint4* Wv = reinterpret_cast<const uint4*>(a.W);
+    const bool tiled = a.w_tiled != 0;
+    size_t wb[4];
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) {
       const int u = u0 + nt * 8 + g;
       const int t = u < U ? a.union_ids[u] : -1;
-      wr[nt] = reinterpret_cast<const uint4*>(a.W + (size_t)((t >= 0 && t < a.V) ? t : 0) * d) + c;
+      wb[nt] = w_row_base((t >= 0 && t < a.V) ? t : 0, d, tiled);
     }
     float acc[4][4];
 #pragma unroll
@@ -155,7 +169,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1) restricted_head_kernel(const Re
           A0[j] = hA[v];
           A1[j] = hB[v];
 #pragma unroll
-          for (int nt = 0; nt < 4; ++nt) B[j][nt] = wr[nt][v];
+          for (int nt = 0; nt < 4; ++nt) B[j][nt] = Wv[w_vec(wb[nt], v + c, tiled)];
         }
       }
 #pragma unroll
@@ -378,7 +392,8 @@ __global__ void __launch_bounds__(32 * RS_WARPS) restricted_sets_kernel(const Re
       const int t0 = sa.cand_offsets[c];
       const int t = sa.tok_ids[t0], r = a.tok_row[t0];
       const float z = dot_row(reinterpret_cast<const uint4*>(ra.H) + (size_t)source_row(ra, r) * nvec,
-                              reinterpret_cast<const uint4*>(ra.W) + (size_t)t * nvec, nvec, lane);
+                              reinterpret_cast<const uint4*>(ra.W), w_row_base(t, ra.d, ra.w_tiled != 0),
+                              ra.w_tiled != 0, nvec, lane);
       if (lane == 0) sa.logp[t0] = z - ra.lse_row[r];
     }
   }

@@ -28,6 +28,7 @@ JET_ERR_TIMEOUT = -9
 
 JET_KIND_CHOICE, JET_KIND_BINARY, JET_KIND_ORDINAL = 0, 1, 2
 JET_MODE_FULL, JET_MODE_RESTRICTED = 0, 1
+JET_W_ROWMAJOR, JET_W_TILED = 0, 1
 JET_MAX_UNION = 4096
 
 SET_OUTPUTS = ("logp", "lse", "s", "q", "q_equiv", "decision", "expected", "confidence", "mass")
@@ -70,6 +71,10 @@ def load() -> C.CDLL:
     sets_sig = [P, P, P, I, P, P, I, P, I, P, P, I, F, I, P, I, C.POINTER(_SetOut), P]
     for name in ("jet_score_sets", "jet_score_sets_async", "jet_score_sets_host"):
         getattr(lib, name).argtypes = sets_sig
+    lib.jet_tiled_weights_bytes.argtypes = [P]
+    lib.jet_tiled_weights_bytes.restype = C.c_size_t
+    lib.jet_tile_weights.argtypes = [P, P, P, P]
+    lib.jet_set_weights_layout.argtypes = [P, I]
     for name in ("jet_score_sets_gather", "jet_score_sets_gather_async"):
         getattr(lib, name).argtypes = [P, P, I, P, I, P, P, P, I, P, I, P, P, I, F, I, P, I, C.POINTER(_SetOut), P]
     lib.jet_sync_status.argtypes = [P, P]
@@ -222,6 +227,26 @@ class JetScorer:
         if rc != JET_OK:
             raise JetError(rc, "jet_score_sets_gather")
         return out
+
+    def tile_weights(self, W: torch.Tensor, use: bool = True) -> torch.Tensor:
+        """The tiled copy of W ([ceil(V/128)*128, d] bf16 in 16 KB boxes, rows
+        past V zero) that the head streams fastest; with use=True the scorer's
+        later calls read their W argument in this layout."""
+        _check_dev(W, "W", self.device, _BF16)
+        n = self.lib.jet_tiled_weights_bytes(self._h) // 2
+        Wt = torch.empty(n // self.d, self.d, dtype=W.dtype, device=self.device)
+        rc = self.lib.jet_tile_weights(self._h, _ptr(W), _ptr(Wt), _stream(self.device))
+        if rc != JET_OK:
+            raise JetError(rc, "jet_tile_weights")
+        if use:
+            self.set_weights_layout(JET_W_TILED)
+        return Wt
+
+    def set_weights_layout(self, layout: int) -> None:
+        """How later calls read W: JET_W_ROWMAJOR (default) or JET_W_TILED."""
+        rc = self.lib.jet_set_weights_layout(self._h, int(layout))
+        if rc != JET_OK:
+            raise JetError(rc, "jet_set_weights_layout")
 
     KERNELS = ("prep", "head", "merge", "restricted", "sets")
 

@@ -42,6 +42,7 @@
 #ifndef JETSCORE_H
 #define JETSCORE_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -81,6 +82,28 @@ enum { JET_MODE_FULL = 0, JET_MODE_RESTRICTED = 1 };
  * On success *out owns the workspace until jet_destroy.
  */
 int jet_create(jet_ctx **out, int d, int V, int max_rows, int max_tokens, int device);
+
+/*
+ * Tiled weights.  The head streams W in 128-row x 64-column boxes; stored
+ * row-major each box is 128 pieces of 128 bytes, 2*d bytes apart.  A tiled copy
+ * puts every box in 16 contiguous KB: element (v, k) of W sits at
+ *   ((floor(v/128) * (d/64) + floor(k/64)) * 128 + v mod 128) * 64 + k mod 64
+ * of a [ceil(V/128) * 128, d] bf16 array (rows past V are zero).  Results are
+ * bit-identical to the row-major layout; the head reads it slightly faster.
+ *
+ * jet_tiled_weights_bytes: size of the tiled copy.
+ * jet_tile_weights: write the tiled copy of W (device, row-major [V, d]) to
+ *   W_tiled (device, jet_tiled_weights_bytes bytes, 16-byte aligned, not
+ *   overlapping W).  Enqueued on `cuda_stream`; returns after enqueueing.
+ * jet_set_weights_layout: how this context's later calls read their W
+ *   argument: JET_W_ROWMAJOR (default) or JET_W_TILED (a jet_tile_weights copy).
+ *   jet_score_tokens_noalloc always reads row-major W.
+ * Errors: JET_ERR_ARG (NULL, alignment, overlap, unknown layout), JET_ERR_CUDA.
+ */
+enum { JET_W_ROWMAJOR = 0, JET_W_TILED = 1 };
+size_t jet_tiled_weights_bytes(const jet_ctx *ctx);
+int jet_tile_weights(jet_ctx *ctx, const void *W_bf16, void *W_tiled_bf16, void *cuda_stream);
+int jet_set_weights_layout(jet_ctx *ctx, int layout);
 
 /* Free the context and its workspace (waits for the device).  NULL is a no-op. */
 void jet_destroy(jet_ctx *ctx);
