@@ -61,6 +61,18 @@ bool head_use_pair(int N) {
   return N > BM;
 }
 
+// Dynamic unit order for the paired head when the schedule has more than one
+// wave of units (JETSCORE_HEAD_DYN=0: fixed stride, diagnostics).
+bool head_use_dynamic(const Plan& p) {
+  static int env = -2;
+  if (env == -2) {
+    const char* v = std::getenv("JETSCORE_HEAD_DYN");
+    env = v ? std::atoi(v) : -1;
+  }
+  if (env == 0) return false;
+  return p.pair && p.units > p.grid / 2;
+}
+
 int head_prefetch_kblocks(const Plan& p) {
   static int env = -2;
   if (env == -2) {
@@ -253,6 +265,7 @@ int run_full_head(jet_ctx* c, const void* H, const void* W, int n_rows, float* l
   ha.err = c->err;
   ha.pf_kblocks = head_prefetch_kblocks(ha.plan);
   ha.w_tiled = c->w_layout == JET_W_TILED ? 1 : 0;
+  ha.sched = head_use_dynamic(plan) ? c->err + SCHED_WORD : nullptr;
   cudaError_t e;
   {
     ProfScope ps(c, K_HEAD, st);
@@ -488,7 +501,7 @@ int jet_create(jet_ctx** out, int d, int V, int max_rows, int max_tokens, int de
   A(dalloc(&c->fit_res, 3));
   A(cudaMallocHost(reinterpret_cast<void**>(&c->h_fit), 3 * sizeof(double)));
   A(cudaMallocHost(reinterpret_cast<void**>(&c->h_err), 2 * ERR_WORDS * sizeof(int)));   // + result words
-  A(cudaMemset(c->err, 0, ERR_WORDS * sizeof(int)));
+  A(cudaMemset(c->err, 0, (SCHED_WORD + 1) * sizeof(int)));
   if (e != cudaSuccess) {
     jet_destroy(c);
     return JET_ERR_CUDA;

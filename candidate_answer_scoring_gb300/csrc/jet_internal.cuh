@@ -28,13 +28,16 @@ struct HeadShape {
   static constexpr int B_BYTES = B_ROWS * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = PAIR ? 6 : 4;          // shared-memory ring depth (7 measured no faster)
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 512 /*barriers, unit ring*/;
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 };
 
 // Device-side error word layout: err[0] = first status (0 = ok),
 // err[1] = index of the offending element, err[2] = where a wait gave up.
 constexpr int ERR_WORDS = 4;
+// err[SCHED_WORD]: the head's unit counter when units are handed out
+// dynamically; the pre-pass zeroes it together with the error words.
+constexpr int SCHED_WORD = ERR_WORDS;
 
 __device__ __forceinline__ void set_error(int* err, int code, int detail) {
   if (atomicCAS(err, 0, code) == 0) err[1] = detail;
@@ -97,10 +100,13 @@ struct HeadArgs {
   int* err;
   int pf_kblocks;       // L2 prefetch distance for W, in k-blocks of the CTA's stream (0: off)
   int w_tiled = 0;      // tmW is the 4-D map of a tiled W (jet_tile_weights)
+  int* sched = nullptr; // paired head, several waves of units: counter (zeroed by the pre-pass)
+                        // from which pairs take units after their first; NULL: static stride
 };
 
 // Host: schedule for N rows on G SMs; units * (1 + pair) <= units_cap.
 Plan make_plan(int N, int V, int d, int G, int units_cap, bool pair);
+bool head_use_dynamic(const Plan& p);
 
 // Host: whether the paired (2-SM) head serves N rows.
 bool head_use_pair(int N);

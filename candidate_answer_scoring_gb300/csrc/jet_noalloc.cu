@@ -146,6 +146,7 @@ extern "C" int jet_score_tokens_noalloc(const void* H, const void* W, int d, int
   ha.part = part;
   ha.err = err;
   ha.pf_kblocks = head_prefetch_kblocks(ha.plan);
+  ha.sched = head_use_dynamic(plan) ? err + SCHED_WORD : nullptr;
   if (launch_head(tmH, tmW, ha, st) != cudaSuccess) {
     cudaStreamSynchronize(st);
     return JET_ERR_CUDA;

@@ -141,6 +141,94 @@ __device__ __forceinline__ void settle_ns(unsigned long long ns) {
   }
 }
 
+// ---- unit ring (paired head, dynamic schedule) ------------------------------------
+// With several waves of units, the pairs take units in order from a global
+// counter instead of a fixed stride, so that the units running at any moment
+// stay neighbours in the schedule (the same band of row tiles, adjacent
+// vocabulary splits) however unevenly the pairs progress; their shared H and W
+// tiles are then still in L2.  The issuing CTA's producer takes each unit id
+// and publishes it in a small ring held by both CTAs; its MMA thread and the
+// epilogue warps, and the second CTA's producer and epilogue warps, read it
+// from there and free the slot on the issuing CTA's barrier.
+constexpr int UR = 4;                           // ring slots
+constexpr int UR_CONSUMERS = 2 * (1 + EPI_WARPS);   // per slot: see above
+
+__device__ __forceinline__ bool mbar_try_wait_acq_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// mbar_wait with cluster-scope acquire: data stored by the other CTA before its
+// release-arrive is visible afterwards.  Bounded like mbar_wait.
+__device__ __noinline__ bool mbar_wait_acq_cluster(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                                   int* err, int where, unsigned long long limit_ns) {
+  const uint32_t a = smem_u32(bar);
+  const unsigned long long t0 = globaltimer();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait_acq_cluster(a, parity)) return true;
+    if ((it & 63u) == 63u) {
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > limit_ns) {
+        *abort_flag = 1;
+        if (err != nullptr && atomicCAS(err, 0, JET_ERR_TIMEOUT) == 0) err[2] = where;
+        return false;
+      }
+    }
+  }
+}
+
+// Issuing CTA's producer: publish unit u at ring position ui in both CTAs,
+// once every consumer has read the slot's previous id.
+__device__ __forceinline__ bool ring_publish(volatile int* uring, uint64_t* ufull, uint64_t* uempty, uint32_t ui,
+                                             int u, volatile int* abort_flag, int* err, unsigned long long limit) {
+  const uint32_t slot = ui % UR, ph = (ui / UR) & 1u;
+  if (!mbar_wait_acq_cluster(&uempty[slot], ph ^ 1u, abort_flag, err, 8, limit)) return false;
+  uring[slot] = u;
+  mbar_arrive(&ufull[slot]);   // release (CTA scope): this CTA's consumers see the id
+  const uint32_t remote = cluster_addr(const_cast<int*>(&uring[slot]), 1);
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(remote), "r"(u) : "memory");
+  mbar_arrive_cluster(&ufull[slot], 1);   // release (cluster scope): orders the store above
+  return true;
+}
+
+// Consumer (one thread): the unit id at ring position ui; frees the slot on
+// the issuing CTA's barrier.  INT_MAX (and ok = false) when the wait fails.
+__device__ __forceinline__ int ring_take(volatile int* uring, uint64_t* ufull, uint64_t* uempty, uint32_t ui,
+                                         bool in_issuer, volatile int* abort_flag, int* err, bool& ok,
+                                         unsigned long long limit) {
+  const uint32_t slot = ui % UR, ph = (ui / UR) & 1u;
+  if (!mbar_wait_acq_cluster(&ufull[slot], ph, abort_flag, err, 9, limit)) {
+    ok = false;
+    return INT_MAX;
+  }
+  const int u = uring[slot];
+  if (in_issuer) mbar_arrive(&uempty[slot]);
+  else mbar_arrive_cluster(&uempty[slot], 0);
+  return u;
+}
+
+// ring_take for a whole warp: lane 0 takes the id, every lane returns it.
+__device__ __forceinline__ int ring_take_warp(volatile int* uring, uint64_t* ufull, uint64_t* uempty, uint32_t ui,
+                                              bool in_issuer, volatile int* abort_flag, int* err, bool& ok,
+                                              unsigned long long limit) {
+  int u = 0, good = 1;
+  if ((threadIdx.x & 31) == 0) {
+    bool o = true;
+    u = ring_take(uring, ufull, uempty, ui, in_issuer, abort_flag, err, o, limit);
+    good = o ? 1 : 0;
+  }
+  u = __shfl_sync(0xffffffffu, u, 0);
+  if (!__shfl_sync(0xffffffffu, good, 0)) ok = false;
+  return u;
+}
+
 // ---- tcgen05 ------------------------------------------------------------------
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -295,14 +383,18 @@ __global__ void __launch_bounds__(HEAD_THREADS, 1)
   uint64_t* tempty = tfull + 2;           // [2] epilogue(s) -> MMA
   uint64_t* drain = tempty + 2;           // [1] MMA drain on abort
   uint64_t* exitb = drain + 1;            // [1] paired exit handshake
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(exitb + 1);
+  uint64_t* ufull = exitb + 1;            // [UR] unit ring: id published
+  uint64_t* uempty = ufull + UR;          // [UR] unit ring: id read by every consumer (issuing CTA's)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(uempty + UR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* uring = abort_flag + 1;   // [UR] unit ids
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = PAIR ? cluster_rank() : 0u;   // CTA within the pair; 0 issues the MMAs
   const bool issuer = rank == 0;
   const int unit0 = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
   const int unit_step = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  const bool dyn = PAIR && a.sched != nullptr;   // units after the first come from the ring
   // No early launch_dependents here: the merge kernel is launched when this
   // grid completes.  Launched early, its CTAs pile onto the SMs the head
   // leaves free and run there several times slower than when spread over all
@@ -319,6 +411,10 @@ __global__ void __launch_bounds__(HEAD_THREADS, 1)
     }
     mbar_init(drain, 1);
     mbar_init(exitb, 1);
+    for (int i = 0; i < UR; ++i) {
+      mbar_init(&ufull[i], 1);
+      mbar_init(&uempty[i], UR_CONSUMERS);
+    }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -345,7 +441,14 @@ __global__ void __launch_bounds__(HEAD_THREADS, 1)
       const uint64_t pol_w = P.n_mt == 1 ? l2_policy_evict_first() : l2_policy_evict_last();
       const uint64_t pol_h = l2_policy_evict_last();
       bool ok = true;
-      for (int u = unit0; ok && u < P.units; u += unit_step) {
+      uint32_t ui = 0;   // unit ring position
+      int u = unit0;
+      if (dyn) {
+        if (issuer) ok = ring_publish(uring, ufull, uempty, ui, u, abort_flag, a.err, WAIT_LIMIT_NS);
+        else u = ring_take(uring, ufull, uempty, ui, false, abort_flag, a.err, ok, WAIT_LIMIT_NS);
+        ++ui;
+      }
+      while (ok && u < P.units) {
         int m, vt0, vt1;
         plan_unit(P, u, m, vt0, vt1);
         const int a_row = m * tile_rows + (int)rank * BM;
@@ -376,6 +479,18 @@ __global__ void __launch_bounds__(HEAD_THREADS, 1)
             if (++stage == NST) { stage = 0; phase ^= 1u; }
           }
         }
+        if (!ok) break;
+        if (!dyn) {
+          u += unit_step;
+        } else if (issuer) {
+          if (ui == 1) pdl_wait();   // the pre-pass zeroes the counter
+          u = unit_step + atomicAdd(a.sched, 1);
+          ok = ring_publish(uring, ufull, uempty, ui, u, abort_flag, a.err, WAIT_LIMIT_NS);
+          ++ui;
+        } else {
+          u = ring_take(uring, ufull, uempty, ui, false, abort_flag, a.err, ok, WAIT_LIMIT_NS);
+          ++ui;
+        }
       }
       if (ok) {
         // tail: wait until the MMA has released every stage, so that no
@@ -403,7 +518,9 @@ __global__ void __launch_bounds__(HEAD_THREADS, 1)
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true, any = false;
-      for (int u = unit0; ok && u < P.units; u += unit_step) {
+      uint32_t ui = 0;
+      int u = dyn ? ring_take(uring, ufull, uempty, ui++, true, abort_flag, a.err, ok, WAIT_LIMIT_NS) : unit0;
+      while (ok && u < P.units) {
         int m, vt0, vt1;
         plan_unit(P, u, m, vt0, vt1);
         for (int vt = vt0; ok && vt < vt1; ++vt) {
@@ -427,6 +544,8 @@ __global__ void __launch_bounds__(HEAD_THREADS, 1)
           acc ^= 1;
           if (acc == 0) acc_phase ^= 1u;
         }
+        if (!ok) break;
+        u = dyn ? ring_take(uring, ufull, uempty, ui++, true, abort_flag, a.err, ok, WAIT_LIMIT_NS) : u + unit_step;
       }
       if (!ok && any) {   // wait until every MMA issued so far has completed
         volatile int never = 0;
@@ -444,7 +563,10 @@ __global__ void __launch_bounds__(HEAD_THREADS, 1)
     pdl_wait();   // row lists and the error word come from the pre-pass
     bool ok = *(volatile const int*)a.err == 0;
     if (!ok) *abort_flag = 1;   // pre-pass rejected the batch: every role stops
-    for (int u = unit0; ok && u < P.units; u += unit_step) {
+    uint32_t ui = 0;
+    int u = unit0;
+    if (dyn && ok) u = ring_take_warp(uring, ufull, uempty, ui++, issuer, abort_flag, a.err, ok, WAIT_LIMIT_NS);
+    while (ok && u < P.units) {
       int m, vt0, vt1;
       plan_unit(P, u, m, vt0, vt1);
       const int row = m * tile_rows + (int)rank * BM + row_in_tile;
@@ -511,6 +633,9 @@ __global__ void __launch_bounds__(HEAD_THREADS, 1)
         if (acc == 0) acc_phase ^= 1u;
       }
       if (ok && valid) a.part[part_slot(P, u, (int)rank, half, row_in_tile)] = make_float2(m_run, s_run);
+      if (!ok) break;
+      u = dyn ? ring_take_warp(uring, ufull, uempty, ui++, issuer, abort_flag, a.err, ok, WAIT_LIMIT_NS)
+              : u + unit_step;
     }
   }
 

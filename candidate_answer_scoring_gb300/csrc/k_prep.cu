@@ -41,7 +41,7 @@ __global__ void __launch_bounds__(PREP_THREADS) prep_kernel(PrepArgs a) {
   const bool identity = a.tok_row == nullptr;    // token i is predicted by row i
 
   if (tid == 0) {
-    for (int i = 0; i < ERR_WORDS; ++i) err[i] = 0;
+    for (int i = 0; i <= SCHED_WORD; ++i) err[i] = 0;   // error words and the head's unit counter
     s_unsorted = 0;
   }
   __syncthreads();

@@ -1,0 +1,76 @@
+"""Unit order of the paired head when its schedule has many waves of units.
+
+With more units than CTA pairs, pairs take their later units in order from a
+counter that the pre-pass resets on every call.  A batch of ~22k rows over a
+small vocabulary (d = 128, V = 2100: 9 vocabulary tiles, 86 row tiles) runs
+about ten waves.  It is compared with the oracle, run three times in one
+process (the counter must start from zero on every call), and compared bit
+for bit with the fixed-stride order (JETSCORE_HEAD_DYN=0), which computes
+every unit's partials the same way on another pair."""
+import os
+import subprocess
+import sys
+import tempfile
+
+import numpy as np
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+sys.path.insert(0, os.path.join(ROOT, "tests"))
+
+import workloads as wk  # noqa: E402
+
+WL_ARGS = dict(d=128, V=2100, n_sets=1000, K=(3, 8), length=(2, 6), kinds=(0,), dup_prob=0.15, seed=41)
+
+SCRIPT = r"""
+import sys, json
+sys.path.insert(0, {root!r})
+import numpy as np, torch
+import workloads as wk
+import candidate_answer_scoring_gb300 as jet
+wl = wk.custom(**{wl_args!r})
+t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+sc = jet.JetScorer(wl.d, wl.V, wl.N, wl.n_tok)
+info = sc.plan_info(wl.N)
+args = (t(wl.H.view(np.int16)).view(torch.bfloat16), t(wl.W.view(np.int16)).view(torch.bfloat16),
+        t(wl.tok_row), t(wl.tok_ids), t(wl.cand_offsets), t(wl.set_offsets), t(wl.kind), wl.T, wl.mode, None)
+runs = []
+for _ in range(3):
+    out = sc.score_sets(*args)
+    torch.cuda.synchronize()
+    runs.append({{k: v.cpu().numpy() for k, v in out.items()}})
+for r in runs[1:]:
+    for k in runs[0]:
+        assert np.array_equal(runs[0][k], r[k], equal_nan=True), ("repeat differs", k)
+np.savez({out!r}, **runs[0])
+print(json.dumps(info))
+"""
+
+
+def _run(env, path):
+    code = SCRIPT.format(root=ROOT, wl_args=WL_ARGS, out=path)
+    r = subprocess.run([sys.executable, "-c", code], env={**os.environ, **env}, capture_output=True, text=True,
+                       timeout=900)
+    assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-4000:]
+    import json
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def test_many_waves_dynamic_order_matches_oracle_and_fixed_order():
+    import oracle
+    from parity import compare
+
+    wl = wk.custom(**WL_ARGS)
+    with tempfile.TemporaryDirectory() as tmp:
+        p_dyn, p_fix = os.path.join(tmp, "dyn.npz"), os.path.join(tmp, "fix.npz")
+        info = _run({}, p_dyn)
+        assert info["tile_rows"] == 256, info               # paired head
+        assert info["units"] > info["ctas"] // 2 * 5, info  # several waves of units
+        _run({"JETSCORE_HEAD_DYN": "0"}, p_fix)
+        dyn, fix = dict(np.load(p_dyn)), dict(np.load(p_fix))
+    for k in dyn:
+        assert np.array_equal(dyn[k], fix[k], equal_nan=True), k
+    compare(wl, dyn, oracle.score_workload(wl))
