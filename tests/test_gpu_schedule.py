@@ -74,3 +74,45 @@ def test_many_waves_dynamic_order_matches_oracle_and_fixed_order():
     for k in dyn:
         assert np.array_equal(dyn[k], fix[k], equal_nan=True), k
     compare(wl, dyn, oracle.score_workload(wl))
+
+
+ERR_SCRIPT = r"""
+import sys, time
+sys.path.insert(0, {root!r})
+import numpy as np, torch
+import workloads as wk
+import candidate_answer_scoring_gb300 as jet
+wl = wk.custom(**{wl_args!r})
+t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+sc = jet.JetScorer(wl.d, wl.V, wl.N, wl.n_tok)
+H = t(wl.H.view(np.int16)).view(torch.bfloat16)
+W = t(wl.W.view(np.int16)).view(torch.bfloat16)
+rest = (t(wl.cand_offsets), t(wl.set_offsets), t(wl.kind), wl.T, wl.mode, None)
+good = sc.score_sets(H, W, t(wl.tok_row), t(wl.tok_ids), *rest)
+good = {{k: v.cpu().numpy() for k, v in good.items()}}
+bad_ids = wl.tok_ids.copy()
+bad_ids[len(bad_ids) // 2] = wl.V                      # one id outside [0, V)
+t0 = time.time()
+try:
+    sc.score_sets(H, W, t(wl.tok_row), t(bad_ids), *rest)
+    raise SystemExit("no error raised")
+except jet.JetError as e:
+    assert e.status == jet.JET_ERR_TOKEN_RANGE, e.status
+dt = time.time() - t0
+assert dt < 1.0, ("the rejected call waited", dt)   # no role sat out a bounded wait
+again = sc.score_sets(H, W, t(wl.tok_row), t(wl.tok_ids), *rest)
+for k, v in again.items():
+    assert np.array_equal(v.cpu().numpy(), good[k], equal_nan=True), ("after the error", k)
+print("ok", round(dt, 3))
+"""
+
+
+def test_many_waves_rejected_batch_stops_promptly_and_context_recovers():
+    """A token id outside [0, V) in a many-wave batch: the pre-pass records
+    JET_ERR_TOKEN_RANGE, every role of every pair stops at its next check
+    (no bounded wait runs out), and the next valid call on the same context
+    reproduces the earlier outputs bit for bit."""
+    code = ERR_SCRIPT.format(root=ROOT, wl_args=WL_ARGS)
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-4000:]
+    assert r.stdout.strip().startswith("ok"), r.stdout

@@ -63,3 +63,30 @@ def test_noalloc_rejects_batches_beyond_its_static_scratch():
     rc = fn(C.c_void_p(H.data_ptr()), C.c_void_p(W.data_ptr()), 64, 100, C.c_void_p(tok.data_ptr()), n,
             C.c_void_p(out.data_ptr()), None, C.c_void_p(torch.cuda.current_stream(dev).cuda_stream))
     assert rc == -6, f"expected JET_ERR_WORKSPACE, got {rc}"
+
+
+def test_noalloc_many_waves_matches_fp32_torch():
+    """4096 positions over V = 30000: 16 paired row tiles and several waves of
+    units (taken in counter order), against logits formed with torch in fp32
+    from the same bf16 values."""
+    jet, fn = _noalloc_fn()
+    dev = torch.device("cuda", 0)
+    d, V, n = 128, 30000, 4096
+    rng = np.random.default_rng(11)
+    W = torch.from_numpy(wk.gen_W(611, V, d).view(np.int16)).to(dev).view(torch.bfloat16)
+    H = torch.from_numpy(wk.to_bf16_bits(rng.normal(size=(n, d)).astype(np.float32)).view(np.int16))
+    H = H.to(dev).view(torch.bfloat16)
+    tok = torch.from_numpy(rng.integers(0, V, size=n).astype(np.int32)).to(dev)
+    info = jet.JetScorer(d, V, n, n).plan_info(n)
+    assert info["units"] > info["ctas"] // 2, info      # more than one wave
+    logp = torch.full((n,), float("nan"), device=dev)
+    lse = torch.full((n,), float("nan"), device=dev)
+    rc = fn(C.c_void_p(H.data_ptr()), C.c_void_p(W.data_ptr()), d, V, C.c_void_p(tok.data_ptr()), n,
+            C.c_void_p(logp.data_ptr()), C.c_void_p(lse.data_ptr()),
+            C.c_void_p(torch.cuda.current_stream(dev).cuda_stream))
+    assert rc == 0, jet.status_string(rc)
+    z = H.float() @ W.float().T
+    ref_lse = torch.logsumexp(z, dim=1)
+    ref_lp = z.gather(1, tok.long()[:, None])[:, 0] - ref_lse
+    assert (lse - ref_lse).abs().max().item() <= TOL
+    assert (logp - ref_lp).abs().max().item() <= TOL
