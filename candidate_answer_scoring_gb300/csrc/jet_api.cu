@@ -145,7 +145,7 @@ struct jet_ctx {
   int* h_err = nullptr;   // pinned
   // row deduplication workspace
   unsigned long long *dd_hash = nullptr, *dd_keys = nullptr;
-  int *dd_vals = nullptr, *dd_rep = nullptr, *dd_rank = nullptr;
+  int *dd_vals = nullptr, *dd_rep = nullptr, *dd_rank = nullptr, *dd_tiles = nullptr;
   int dd_table = 0;
   // temperature fitting
   double *fit_res = nullptr, *h_fit = nullptr;   // device [3], pinned host [3]
@@ -498,6 +498,7 @@ int jet_create(jet_ctx** out, int d, int V, int max_rows, int max_tokens, int de
   A(dalloc(&c->dd_vals, (size_t)c->dd_table));
   A(dalloc(&c->dd_rep, R));
   A(dalloc(&c->dd_rank, R + 1));
+  A(dalloc(&c->dd_tiles, R / 1024 + 1));
   A(dalloc(&c->fit_res, 3));
   A(cudaMallocHost(reinterpret_cast<void**>(&c->h_fit), 3 * sizeof(double)));
   A(cudaMallocHost(reinterpret_cast<void**>(&c->h_err), 2 * ERR_WORDS * sizeof(int)));   // + result words
@@ -517,7 +518,7 @@ void jet_destroy(jet_ctx* c) {
   void* ptrs[] = {c->io_dev, c->row_ptr, c->row_cur, c->row_list, c->iscratch, c->lse_row, c->umap, c->zu, c->zg, c->part, c->hash,
                   c->lse, c->logp, c->s, c->q, c->qe, c->dec, c->expd, c->conf, c->mass, c->stH,
                   c->d_in,
-                  c->dd_hash, c->dd_keys, c->dd_vals, c->dd_rep, c->dd_rank};
+                  c->dd_hash, c->dd_keys, c->dd_vals, c->dd_rep, c->dd_rank, c->dd_tiles};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   for (auto& v : c->ev)
@@ -559,6 +560,7 @@ int jet_dedup_rows(jet_ctx* c, const void* H, int n_rows, const int32_t* tok_row
   a.table = table;
   a.rep = c->dd_rep;
   a.rank = c->dd_rank;
+  a.tile_count = c->dd_tiles;
   a.err = c->err;
   if (launch_dedup(a, st) != cudaSuccess) {
     cudaStreamSynchronize(st);

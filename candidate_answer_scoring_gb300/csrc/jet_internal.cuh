@@ -232,6 +232,7 @@ struct DedupArgs {
   int table;                  // power of two >= 2 * n_rows
   int* rep;                   // [n_rows]
   int* rank;                  // [n_rows + 1]; rank[n_rows] = distinct rows
+  int* tile_count;            // [ceil(n_rows / 1024)] representatives per 1024-row tile
   int* err;
 };
 cudaError_t launch_dedup(const DedupArgs& a, cudaStream_t st);

@@ -42,9 +42,11 @@ def run_dedup(jet, sc, wl):
     return Hu.view(torch.int16).cpu().numpy().view(np.uint16), tok_u.cpu().numpy(), row_map.cpu().numpy()
 
 
-@pytest.mark.parametrize("case", ["custom-dups", "multitoken", "no-dups", "all-equal"])
+@pytest.mark.parametrize("case", ["custom-dups", "multitoken", "no-dups", "all-equal", "large"])
 def test_dedup_is_exact(jet, case):
-    if case == "custom-dups":
+    if case == "large":                 # 20026 rows of d = 4096: 20 rank tiles of 1024 rows
+        wl = wk.large_choice()
+    elif case == "custom-dups":
         wl = wk.custom(128, 900, 40, K=(2, 8), length=(1, 6), dup_prob=0.3, seed=31)
     elif case == "multitoken":
         wl = wk.multi_token_choice()
@@ -98,3 +100,34 @@ def test_dedup_rejects_bad_input(jet):
     assert e.value.status == -1
     Hu, tok_u, _ = sc.dedup_rows(H, dev(wl.tok_row))                   # context still works
     assert Hu.shape[0] >= 1
+
+
+@pytest.mark.parametrize("n", [1023, 1024, 1025, 2048, 2049])
+def test_dedup_rank_tile_edges(jet, n):
+    """Row counts at and around the rank pass's 1024-row tiles: the leading n
+    rows of the multitoken batch (shared histories repeat rows across tiles),
+    one token per row."""
+    base = wk.multi_token_choice()
+    H = np.ascontiguousarray(base.H[:n])
+    sc = jet.JetScorer(base.d, base.V, n, n)
+    Hd = dev(H.view(np.int16)).view(torch.bfloat16)
+    Hu, tok_u, row_map = sc.dedup_rows(Hd, dev(np.arange(n, dtype=np.int32)), want_row_map=True)
+    torch.cuda.synchronize()
+    rep, order = first_occurrence(H)
+    assert order.size < n                                  # the prefix holds duplicates
+    np.testing.assert_array_equal(Hu.view(torch.int16).cpu().numpy().view(np.uint16), H[order])
+    np.testing.assert_array_equal(row_map.cpu().numpy(), rep)
+    np.testing.assert_array_equal(tok_u.cpu().numpy(), rep)
+
+
+def test_dedup_without_tokens(jet):
+    """No token rows to remap (n_tok = 0): rows are still compacted."""
+    wl = wk.custom(64, 300, 5, K=(2, 4), length=(1, 3), dup_prob=0.5, seed=4)
+    sc = jet.JetScorer(wl.d, wl.V, wl.N, wl.n_tok)
+    H = dev(wl.H.view(np.int16)).view(torch.bfloat16)
+    Hu, tok_u, row_map = sc.dedup_rows(H, torch.empty(0, dtype=torch.int32, device="cuda"), want_row_map=True)
+    torch.cuda.synchronize()
+    rep, order = first_occurrence(wl.H)
+    np.testing.assert_array_equal(Hu.view(torch.int16).cpu().numpy().view(np.uint16), wl.H[order])
+    np.testing.assert_array_equal(row_map.cpu().numpy(), rep)
+    assert tok_u.numel() == 0

@@ -217,6 +217,45 @@ def test_shape_extremes(jet, case):
             assert np.all(gpu["logp"] == 0.0) and np.all(gpu["q"] == 1.0)
 
 
+@pytest.mark.parametrize("T", [0.02, 0.25, 50.0])
+def test_temperature_extremes(jet, T):
+    """Set rules at temperatures from one-hot (0.02: most q underflow to 0) to
+    flat (50); mass stays at T = 1.
+
+    T = 50 meets the standard tolerances.  Below T = 1 the set softmax
+    magnifies the score error: with da = max |s_gpu - s_oracle| / T over a set
+    of K, the softmax Jacobian bounds |dq_i| by da / 2, |d expected| by
+    (K - 1) da, |d q_equiv| by da (a group's q changes by at most the total
+    variation, da), and |d confidence| by 2 da (1 + ln K) / ln K
+    (d(-q ln q) = -(1 + ln q) dq with dq_i = q_i (da_i - <da>)).  Those bounds
+    replace the fixed ones; decisions stay exact wherever the oracle's margin
+    exceeds 1e-3."""
+    wl = wk.custom(128, 2300, 60, K=(2, 8), length=(1, 4), dup_prob=0.15, T=T, seed=31)
+    gpu = run_gpu(jet, wl)
+    orc = oracle.score_workload(wl)
+    if T > 1:
+        compare(wl, gpu, orc)
+        return
+    from parity import LOGP_ATOL, MARGIN, MASS_ATOL
+    assert np.abs(gpu["logp"].astype(np.float64) - orc.logp).max() <= LOGP_ATOL
+    lens = np.diff(wl.cand_offsets)
+    ds = np.abs(gpu["s"].astype(np.float64) - orc.s)
+    assert np.all(ds <= LOGP_ATOL * lens)
+    assert np.abs(gpu["mass"].astype(np.float64) - orc.mass).max() <= MASS_ATOL
+    for k in range(wl.n_sets):
+        c0, c1 = wl.set_offsets[k], wl.set_offsets[k + 1]
+        K = c1 - c0
+        da = ds[c0:c1].max() / T + 1e-5          # + fp32 rounding of q itself
+        assert np.abs(gpu["q"][c0:c1] - orc.q[c0:c1]).max() <= da / 2, k
+        assert np.abs(gpu["q_equiv"][c0:c1] - orc.q_equiv[c0:c1]).max() <= da, k
+        assert abs(gpu["expected"][k] - orc.expected[k]) <= (K - 1) * da, k
+        if K > 1:
+            assert abs(gpu["confidence"][k] - orc.confidence[k]) <= 2 * da * (1 + np.log(K)) / np.log(K), k
+        if orc.margin[k] > MARGIN:
+            assert gpu["decision"][k] == orc.decision[k], k
+    assert np.all(np.isfinite(gpu["q"])) and np.all(np.abs(gpu["q"].reshape(-1)).max() <= 1.0)
+
+
 def test_repeat_calls_are_bitwise_deterministic(jet):
     wl = wk.custom(128, 2500, 30, K=(2, 8), length=(1, 5), seed=21)
     sc = jet.JetScorer(wl.d, wl.V, wl.N, wl.n_tok)
