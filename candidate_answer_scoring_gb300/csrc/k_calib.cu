@@ -14,9 +14,13 @@
 // One CTA of 1024 threads: each thread evaluates (loss, gradient, curvature)
 // of sets t, t+1024, ... in fp32 (fp64 arithmetic is slow on this part, so it
 // is kept to the sums over sets), warps combine in a fixed butterfly, thread 0
-// sums the warps in order and takes a Newton step on beta, kept inside a
-// shrinking bracket [lo, hi] that bisection falls back to; iterate until the
-// step or the bracket is below 1e-9 relative.  Deterministic.
+// combines the warps (warp 0, fixed butterfly) and takes a Newton step on
+// beta, kept inside a shrinking bracket [lo, hi] that bisection falls back
+// to; iterate until the step or the bracket is below FT_REL_TOL of beta.  The
+// per-set terms carry fp32 rounding, so the gradient summed over sets is
+// known to about 1e-5 absolute against a curvature summed over the same sets:
+// steps below ~1e-8 relative are noise, and a tighter tolerance only walks
+// the bracket in by noise-sized steps.  Deterministic.
 #include "jet_internal.cuh"
 
 namespace jet {
@@ -24,7 +28,9 @@ namespace {
 
 constexpr int FT_THREADS = 1024;
 constexpr int FT_WARPS = FT_THREADS / 32;
+static_assert(FT_WARPS == 32, "the warp partials are combined by one warp");
 constexpr int FT_MAX_IT = 200;
+constexpr double FT_REL_TOL = 1e-7;
 
 __device__ __forceinline__ float wmax(float v) {
 #pragma unroll
@@ -125,22 +131,25 @@ __global__ void __launch_bounds__(FT_THREADS) fit_temperature_kernel(const FitAr
       s_part[warp][2] = Hs;
     }
     __syncthreads();
-    if (tid == 0) {
-      double Lt = 0.0, Gt = 0.0, Ht = 0.0;
-      for (int w = 0; w < FT_WARPS; ++w) {
-        Lt += s_part[w][0];
-        Gt += s_part[w][1];
-        Ht += s_part[w][2];
+    if (warp == 0) {
+      double Lt = s_part[lane][0], Gt = s_part[lane][1], Ht = s_part[lane][2];   // FT_WARPS == 32
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        Lt += __shfl_xor_sync(0xffffffffu, Lt, o);
+        Gt += __shfl_xor_sync(0xffffffffu, Gt, o);
+        Ht += __shfl_xor_sync(0xffffffffu, Ht, o);
       }
-      loss = Lt;
-      if (Gt > 0.0) hi = beta;          // NLL rising in beta: the optimum lies below
-      else lo = beta;
-      double next = (Ht > 0.0) ? beta - Gt / Ht : 0.5 * (lo + hi);
-      if (!(next > lo && next < hi)) next = 0.5 * (lo + hi);
-      const bool done = Gt == 0.0 || fabs(next - beta) <= 1e-9 * beta || (hi - lo) <= 1e-9 * beta ||
-                        it + 1 >= FT_MAX_IT;
-      s_done = done ? 1 : 0;
-      if (!done) s_beta = next;
+      if (lane == 0) {   // thread 0: the bracket and the iterate live here
+        loss = Lt;
+        if (Gt > 0.0) hi = beta;          // NLL rising in beta: the optimum lies below
+        else lo = beta;
+        double next = (Ht > 0.0) ? beta - Gt / Ht : 0.5 * (lo + hi);
+        if (!(next > lo && next < hi)) next = 0.5 * (lo + hi);
+        const bool done = Gt == 0.0 || fabs(next - beta) <= FT_REL_TOL * beta ||
+                          (hi - lo) <= FT_REL_TOL * beta || it + 1 >= FT_MAX_IT;
+        s_done = done ? 1 : 0;
+        if (!done) s_beta = next;
+      }
     }
     __syncthreads();
     if (s_done) break;
