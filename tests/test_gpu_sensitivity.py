@@ -22,22 +22,26 @@ def dev(a):
     return torch.from_numpy(np.ascontiguousarray(a)).cuda()
 
 
-def case(seed, n=40, L=36, const_input=False):
+def case(seed, n=40, L=36, const_input=False, len_range=(2, 66)):
     rng = np.random.default_rng(seed)
-    lens = rng.integers(2, 66, size=n)
+    lens = rng.integers(len_range[0], len_range[1], size=n)
     offsets = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
     total = int(offsets[-1])
     z = rng.normal(-20, 6, size=total).astype(np.float32)
-    if const_input:
+    if const_input:                       # flat logit vectors: rms(ctr(z)) = 0, d = rd / eps
         z[offsets[0]:offsets[1]] = -7.0
+        z[offsets[1]:offsets[2]] = -7.3   # fp32 sums of -7.3 are inexact: flatness must be exact
     scale = np.exp(rng.normal(-2, 1.5, size=L))           # layers differ in how much they move the logits
     z_skip = (z[None, :] + scale[:, None] * rng.normal(size=(L, total)) + rng.normal(size=(L, 1)) * 3).astype(np.float32)
     return z, z_skip, offsets
 
 
-@pytest.mark.parametrize("seed,const_input", [(0, False), (1, False), (2, True)])
-def test_matches_oracle(scorer, seed, const_input):
-    z, z_skip, offsets = case(seed, const_input=const_input)
+@pytest.mark.parametrize("seed,const_input,L,len_range", [
+    (0, False, 36, (2, 66)), (1, False, 36, (2, 66)), (2, True, 36, (2, 66)),
+    (4, False, 9, (200, 600)),     # segments held 8 per lane and, past 256 logits, read in two passes
+])
+def test_matches_oracle(scorer, seed, const_input, L, len_range):
+    z, z_skip, offsets = case(seed, L=L, const_input=const_input, len_range=len_range)
     k = 6
     d, J, sel = scorer.layer_sensitivity(dev(z), dev(z_skip), dev(offsets), k)
     torch.cuda.synchronize()
