@@ -57,10 +57,15 @@ def load_peaks():
     return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
 
 
+# every source the head kernel's translation unit is built from
+HEAD_SOURCES = ("candidate_answer_scoring_gb300/csrc/k_head.cu", "candidate_answer_scoring_gb300/csrc/jet_head.cuh",
+                "candidate_answer_scoring_gb300/csrc/jet_wait.cuh", "include/jetscore.h")
+
+
 def head_source_hash():
     h = hashlib.sha256()
-    for f in ("k_head.cu", "jet_internal.cuh"):
-        h.update(open(os.path.join(ROOT, "candidate_answer_scoring_gb300", "csrc", f), "rb").read())
+    for f in HEAD_SOURCES:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
     return h.hexdigest()[:16]
 
 

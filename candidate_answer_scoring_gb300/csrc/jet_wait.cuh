@@ -5,7 +5,7 @@
 // hanging the GPU.
 #pragma once
 
-#include "jet_internal.cuh"
+#include "jet_head.cuh"
 
 namespace jet {
 namespace {

@@ -35,7 +35,7 @@
 #include <atomic>
 #include <climits>
 
-#include "jet_internal.cuh"
+#include "jet_head.cuh"
 #include "jet_wait.cuh"
 
 namespace jet {
