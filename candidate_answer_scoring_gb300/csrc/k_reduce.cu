@@ -24,6 +24,8 @@ __device__ __forceinline__ void lse_fold(float& m, float& s, float m2, float s2)
   m = mn;
 }
 
+constexpr int MERGE_LOADS = 8;
+
 __global__ void __launch_bounds__(256) merge_kernel(const MergeArgs a) {
   const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -38,20 +40,18 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeArgs a) {
   const int m_tile = r / rows, sub = (r - m_tile * rows) / BM, lr = r % BM;
   float m = -INFINITY, s = 0.f;
   const int n_slots = 2 * P.S;                        // (split, column half) pairs
-  int slot = lane;
-  for (; slot + 96 < n_slots; slot += 128) {        // four independent loads in flight
-    float2 p[4];
+  // rounds of MERGE_LOADS loads per lane, all issued before any is folded
+  // (one L2 round trip per round: up to 256 partials per row in one)
+  for (int base = 0; base < n_slots; base += 32 * MERGE_LOADS) {
+    float2 p[MERGE_LOADS];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int sl = slot + 32 * i;
-      p[i] = a.part[part_slot(P, plan_unit_of(P, m_tile, sl >> 1), sub, sl & 1, lr)];
+    for (int i = 0; i < MERGE_LOADS; ++i) {
+      const int sl = base + lane + 32 * i;
+      p[i] = sl < n_slots ? a.part[part_slot(P, plan_unit_of(P, m_tile, sl >> 1), sub, sl & 1, lr)]
+                          : make_float2(-INFINITY, 0.f);
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) lse_fold(m, s, p[i].x, p[i].y);
-  }
-  for (; slot < n_slots; slot += 32) {
-    const float2 p = a.part[part_slot(P, plan_unit_of(P, m_tile, slot >> 1), sub, slot & 1, lr)];
-    lse_fold(m, s, p.x, p.y);
+    for (int i = 0; i < MERGE_LOADS; ++i) lse_fold(m, s, p[i].x, p[i].y);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {

@@ -14,10 +14,14 @@
 //
 //  1. restricted_head_kernel: z = H U^T is a small dense contraction, run on
 //     the tensor cores with mma.sync (m16n8k16, bf16 in, fp32 accumulate).
-//     One CTA per 16 rows; its 16 warps split d, each accumulating the
-//     16 x 32 tile of a group of 32 codes, and the warps' partials are summed
-//     in a fixed order through shared memory.  Warp r then folds row r's 32
-//     logits into a running (max, sum) for lse_U.  z goes to an [N, |U|]
+//     A cluster of four CTAs per 16 rows splits d four ways (so the union
+//     rows and hidden rows each CTA stages are a quarter, and arrive in one
+//     round of loads); each CTA's 16 warps split its quarter further, each
+//     accumulating the 16 x 32 tile of a group of 32 codes.  The warps'
+//     partials are summed in a fixed order through shared memory, then the
+//     first CTA of the cluster adds the other three CTAs' sums (distributed
+//     shared memory, rank order) and its warp r folds row r's 32 logits into
+//     a running (max, sum) for lse_U.  z goes to an [N, |U|]
 //     scratch when that fits the context's workspace, else the second kernel
 //     recomputes the few logits it needs (a warp dot product: the same bf16
 //     products in fp32, summed in another order).  CTA 0 zeroes the error word
@@ -42,6 +46,7 @@ constexpr int RT_WARPS = 16;                  // warps of the restricted head, s
 constexpr int RT_THREADS = RT_WARPS * 32;     // = 16 rows x 32 codes for the reduction
 constexpr int RT_CODES = 32;                  // codes per group: four n8 tiles
 constexpr int RT_UNROLL = 3;                  // 32-wide k chunks with loads in flight per warp
+constexpr int RT_SPLIT = 4;                   // CTAs of a cluster splitting d for one 16-row tile
 constexpr int DR_BATCH = 10;                  // 16-byte vectors in flight per lane (warp dot product)
 constexpr int RS_WARPS = 8;                   // sets per CTA of the set kernel
 
@@ -112,6 +117,25 @@ __device__ __forceinline__ int source_row(const RestrictedArgs& a, int r) {
   return (idx >= 0 && idx < a.n_src) ? idx : 0;
 }
 
+__device__ __forceinline__ uint32_t rt_cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Every thread of every CTA of the cluster: shared-memory writes before it are
+// visible to the cluster's reads after it.
+__device__ __forceinline__ void rt_cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Store v at the same shared-memory offset as *p in CTA `rank` of the cluster.
+__device__ __forceinline__ void rt_st_cluster(float* p, uint32_t rank, float v) {
+  uint32_t local = static_cast<uint32_t>(__cvta_generic_to_shared(p)), remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+}
+
 // Fragment mapping.  In an m16n8k16 MMA, lane (g = lane/4, c = lane%4) holds
 // A elements (rows g and g+8) and B elements (code g) at k slots {2c, 2c+1,
 // 2c+8, 2c+9}.  A dot product does not care which physical k feeds which slot
@@ -121,10 +145,12 @@ __device__ __forceinline__ int source_row(const RestrictedArgs& a, int r) {
 // a 32-wide chunk (words 0-1: step 0, words 2-3: step 1).
 __global__ void __launch_bounds__(RT_THREADS, 1) restricted_head_kernel(const RestrictedArgs a) {
   __shared__ float sAcc[RT_WARPS][16][RT_CODES + 1];
+  __shared__ float sRecv[RT_SPLIT - 1][16][RT_CODES];   // first CTA: the other CTAs' sums, by rank
   __shared__ float sM[16], sS[16];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, c = lane & 3;
   const int U = a.n_union, d = a.d;
-  const int r0 = blockIdx.x * 16;
+  const uint32_t crank = rt_cluster_rank();
+  const int r0 = (int)(blockIdx.x / RT_SPLIT) * 16;
   pdl_wait();      // earlier work on the stream is complete before any access
   pdl_trigger();
   if (blockIdx.x == 0) {
@@ -139,7 +165,8 @@ __global__ void __launch_bounds__(RT_THREADS, 1) restricted_head_kernel(const Re
   // this lane's two rows (clamped to the last row: loads stay in bounds, the
   // results of rows past N are never written)
   const int nch = d / 32;                                    // 32-wide k chunks
-  const int ch0 = warp * nch / RT_WARPS, ch1 = (warp + 1) * nch / RT_WARPS;
+  const int cs0 = (int)crank * nch / RT_SPLIT, cn = ((int)crank + 1) * nch / RT_SPLIT - cs0;   // this CTA's
+  const int ch0 = cs0 + warp * cn / RT_WARPS, ch1 = cs0 + (warp + 1) * cn / RT_WARPS;
   const uint4* hA = reinterpret_cast<const uint4*>(a.H + (size_t)source_row(a, min(r0 + g, a.N - 1)) * d) + c;
   const uint4* hB = reinterpret_cast<const uint4*>(a.H + (size_t)source_row(a, min(r0 + g + 8, a.N - 1)) * d) + c;
 
@@ -193,12 +220,18 @@ __global__ void __launch_bounds__(RT_THREADS, 1) restricted_head_kernel(const Re
     }
     __syncthreads();
     // warp w now owns row w of the tile, lane = code: sum the warps' partials
-    // in order, store z, fold the group into the row's running (max, sum)
-    {
-      const int row = warp, u = u0 + lane, r = r0 + row;
-      float z = 0.f;
+    // in order; the first CTA adds the others' sums in rank order, stores z
+    // and folds the group into the row's running (max, sum)
+    float zp = 0.f;
 #pragma unroll
-      for (int w = 0; w < RT_WARPS; ++w) z += sAcc[w][row][lane];
+    for (int w = 0; w < RT_WARPS; ++w) zp += sAcc[w][warp][lane];
+    if (crank != 0) rt_st_cluster(&sRecv[crank - 1][warp][lane], 0, zp);
+    rt_cluster_sync();   // the stores above are visible in the first CTA
+    if (crank == 0) {
+      const int row = warp, u = u0 + lane, r = r0 + row;
+      float z = zp;
+#pragma unroll
+      for (int k = 0; k < RT_SPLIT - 1; ++k) z += sRecv[k][row][lane];
       bool valid = u < U;
       if (valid) {
         if (!(t_lane >= 0 && t_lane < a.V)) z = __int_as_float(0x7fc00000);   // reported by the set kernel
@@ -216,9 +249,11 @@ __global__ void __launch_bounds__(RT_THREADS, 1) restricted_head_kernel(const Re
         sM[row] = M;
       }
     }
-    __syncthreads();   // sAcc is reused by the next group
+    // another group reuses sAcc and sRecv: the first CTA has read this one's first
+    if (u0 + RT_CODES < U) rt_cluster_sync();
+    else __syncthreads();
   }
-  if (lane == 0 && r0 + warp < a.N) {
+  if (crank == 0 && lane == 0 && r0 + warp < a.N) {
     const float lse = sM[warp] + logf(sS[warp]);
     a.lse_row[r0 + warp] = lse;
     if (a.lse) a.lse[r0 + warp] = lse;
@@ -405,7 +440,20 @@ __global__ void __launch_bounds__(32 * RS_WARPS) restricted_sets_kernel(const Re
 
 cudaError_t launch_restricted(const RestrictedArgs& a, cudaStream_t st) {
   if (a.N <= 0) return cudaSuccess;
-  return launch_dependent(restricted_head_kernel, dim3((a.N + 15) / 16), dim3(RT_THREADS), 0, st, a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(RT_SPLIT * ((a.N + 15) / 16));
+  cfg.blockDim = dim3(RT_THREADS);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = RT_SPLIT;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, restricted_head_kernel, a);
 }
 
 cudaError_t launch_restricted_sets(const RestrictedSetArgs& a, cudaStream_t st) {
