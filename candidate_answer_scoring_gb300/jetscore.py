@@ -346,3 +346,41 @@ class JetScorer:
         if rc != JET_OK:
             raise JetError(rc, "jet_score_sets_host")
         return out
+
+    def bind_host_call(self, H, W, tok_row, tok_ids, cand_offsets, set_offsets, kind, T: float,
+                       mode: int = JET_MODE_FULL, union_ids=None,
+                       out: Optional[Dict[str, torch.Tensor]] = None):
+        """score_sets_host with its checks and argument marshalling done once:
+        returns (call, out), where call() makes only the jet_score_sets_host
+        C call on the current stream (as a C caller holding these buffers
+        would) and raises JetError on a non-zero status.  The tensors must stay
+        alive and unchanged in shape while call is used; their contents may
+        change between calls."""
+        _check_dev(W, "W", self.device, _BF16)
+        cpu = torch.device("cpu")
+        _check_dev(H, "H", cpu, _BF16)
+        for name, t in (("tok_row", tok_row), ("tok_ids", tok_ids), ("cand_offsets", cand_offsets),
+                        ("set_offsets", set_offsets)):
+            _check_dev(t, name, cpu, (torch.int32,))
+        _check_dev(kind, "kind", cpu, (torch.uint8,))
+        if union_ids is not None:
+            _check_dev(union_ids, "union_ids", cpu, (torch.int32,))
+        if out is None:
+            n = (H.shape[0], tok_ids.numel(), cand_offsets.numel() - 1, set_offsets.numel() - 1)
+            sizes = dict(logp=n[1], lse=n[0], s=n[2], q=n[2], q_equiv=n[2], decision=n[3], expected=n[3],
+                         confidence=n[3], mass=n[3])
+            out = {k: torch.empty(v, dtype=torch.int32 if k == "decision" else torch.float32).pin_memory()
+                   for k, v in sizes.items()}
+        args, keep = self._set_args(H, W, tok_row, tok_ids, cand_offsets, set_offsets, kind, T, mode, union_ids,
+                                    out)
+        args = tuple(args) + (_stream(self.device),)
+        fn = self.lib.jet_score_sets_host
+        held = (H, W, tok_row, tok_ids, cand_offsets, set_offsets, kind, union_ids, out, keep)
+
+        def call():
+            rc = fn(*args)
+            if rc != JET_OK:
+                raise JetError(rc, "jet_score_sets_host")
+            return held
+
+        return call, out

@@ -278,6 +278,30 @@ def test_host_entry_matches_device_entry(jet):
         assert np.array_equal(host[k].numpy().view(np.uint32), dev[k].view(np.uint32)), k
 
 
+def test_bound_host_call_matches_host_entry(jet):
+    """bind_host_call marshals once; each call() is the bare C call on the
+    same buffers, so new contents written into them are scored (here the
+    new hidden rows copied over the first batch's)."""
+    import dataclasses
+    a = wk.custom(128, 1200, 20, K=(2, 6), length=(1, 4), seed=17)
+    rng = np.random.default_rng(18)
+    b = dataclasses.replace(a, H=wk.to_bf16_bits(rng.normal(size=a.H.shape).astype(np.float32)))
+    sc = jet.JetScorer(a.d, a.V, a.N, a.n_tok)
+    W = to_dev(a)["W"]
+    cpu = lambda x: torch.from_numpy(np.ascontiguousarray(x)).pin_memory()
+    H = cpu(a.H.view(np.int16)).view(torch.bfloat16)
+    args = (H, W, cpu(a.tok_row), cpu(a.tok_ids), cpu(a.cand_offsets), cpu(a.set_offsets), cpu(a.kind), a.T)
+    call, out = sc.bind_host_call(*args)
+    ref = sc.score_sets_host(*args)
+    call()
+    for k in OUT_KEYS:
+        assert np.array_equal(out[k].numpy().view(np.uint32), ref[k].numpy().view(np.uint32)), k
+    H.copy_(torch.from_numpy(b.H.view(np.int16)).view(torch.bfloat16))   # new rows, same shapes
+    call()
+    got = {k: v.numpy() for k, v in out.items()}
+    compare(b, got, oracle.score_workload(b))
+
+
 def test_host_entry_restricted_subset_and_errors(jet):
     """The host entry packs the index arrays into one copy in and the requested
     outputs (behind the status words) into one copy out: restricted mode, a
