@@ -11,8 +11,9 @@
 //             segment's elements (coalesced): the input's logits stay in
 //             registers (segments up to 256 logits; longer ones take a
 //             two-pass loop over memory), the layers' segments are loaded
-//             16 values per lane at a time, and means and centred sums of
-//             squares use fixed butterfly reductions; rms(ctr(z)) is exactly
+//             16 values per lane at a time, and the layers' means and centred
+//             sums of squares are reduced together (transpose_reduce, fixed
+//             order); rms(ctr(z)) is exactly
 //             0 for a flat vector; each warp validates its own segment before
 //             reading it;
 //   J pass    one CTA per layer sums its d over inputs in a fixed order;
@@ -44,6 +45,48 @@ __device__ __forceinline__ float wmax_s(float v) {
 }
 
 constexpr int SENS_LG = 8;   // layers per warp in the d pass
+
+// Sums over the warp of SB values per lane (one per layer), SB a power of two
+// <= 32, in 5 + (SB - 1) - log2(SB) shuffles instead of 5 * SB: at each of the
+// first log2(SB) butterfly steps a lane keeps the half of its values that its
+// partner does not and adds the partner's copy; the remaining steps are a
+// plain butterfly.  Afterwards lane l holds the total of value rt_layer<SB>(l).
+// Fixed order: identical inputs give identical sums.
+template <int SB>
+__device__ __forceinline__ float transpose_reduce(float (&v)[SB], int lane) {
+#pragma unroll
+  for (int half = SB / 2, off = 16; half >= 1; half /= 2, off /= 2) {
+    const bool hi = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float send = hi ? v[i] : v[i + half];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, off);
+      v[i] = (hi ? v[i + half] : v[i]) + recv;
+    }
+  }
+  float t = v[0];
+#pragma unroll
+  for (int off = 16 / SB; off >= 1; off /= 2) t += __shfl_xor_sync(0xffffffffu, t, off);
+  return t;
+}
+
+// Which value lane l holds after transpose_reduce<SB>, and a lane holding value u.
+template <int SB>
+__device__ __forceinline__ int rt_layer(int lane) {
+  int u = 0;
+#pragma unroll
+  for (int half = SB / 2, off = 16; half >= 1; half /= 2, off /= 2)
+    if (lane & off) u += half;
+  return u;
+}
+template <int SB>
+__device__ __forceinline__ int rt_lane(int u) {
+  int l = 0;
+#pragma unroll
+  for (int half = SB / 2, off = 16; half >= 1; half /= 2, off /= 2)
+    if (u & half) l += off;
+  return l;
+}
 
 // d for layers [l0, l0 + SENS_LG) of input x, its segment [b, e) held as VPL
 // values per lane (element b + lane + 32 j); the segments of SB layers are
@@ -84,25 +127,31 @@ __device__ __forceinline__ void sens_d_regs(const SensArgs& a, int x, int l0, in
 #pragma unroll
       for (int j = 0; j < VPL; ++j) dv[u][j] = in[j] ? zs[b + lane + 32 * j] : 0.f;
     }
+    float part[SB];
 #pragma unroll
     for (int u = 0; u < SB; ++u) {
-      float sd = 0.f;
+      part[u] = 0.f;
 #pragma unroll
       for (int j = 0; j < VPL; ++j) {
         dv[u][j] = in[j] ? dv[u][j] - zr[j] : 0.f;
-        sd += dv[u][j];
+        part[u] += dv[u][j];
       }
-      const float md = __fdiv_rn(wsum_s(sd), fm);
-      float qd = 0.f;
+    }
+    // lane l now holds the mean of layer rt_layer(l); every lane takes each layer's
+    const float mine = __fdiv_rn(transpose_reduce<SB>(part, lane), fm);
+#pragma unroll
+    for (int u = 0; u < SB; ++u) {
+      const float md = __shfl_sync(0xffffffffu, mine, rt_lane<SB>(u));
+      part[u] = 0.f;
 #pragma unroll
       for (int j = 0; j < VPL; ++j) {
         const float c = in[j] ? dv[u][j] - md : 0.f;
-        qd += c * c;
+        part[u] += c * c;
       }
-      const float rd = sqrtf(wsum_s(qd) * inv_m);
-      const int l = l0 + t0 + u;
-      if (lane == 0 && l < a.L) a.d[(size_t)l * a.n_inputs + x] = rd / rz;
     }
+    const float rd = sqrtf(transpose_reduce<SB>(part, lane) * inv_m);
+    const int l = l0 + t0 + rt_layer<SB>(lane);
+    if (lane == rt_lane<SB>(rt_layer<SB>(lane)) && l < a.L) a.d[(size_t)l * a.n_inputs + x] = rd / rz;
   }
 }
 
