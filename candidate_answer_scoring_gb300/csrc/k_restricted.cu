@@ -136,6 +136,23 @@ __device__ __forceinline__ void rt_st_cluster(float* p, uint32_t rank, float v) 
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
 }
 
+// The union's rows of W are loaded with an L2 evict-last hint: calls that
+// score over the same union find them in L2, although the full-vocabulary
+// head streams all of W through it (with evict-first) in between (binary
+// step: load phase 2.0 -> 1.8 us).
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint4 ld_keep_l2(const uint4* ptr, uint64_t pol) {
+  uint4 v;
+  asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(ptr), "l"(pol));
+  return v;
+}
+
 // Fragment mapping.  In an m16n8k16 MMA, lane (g = lane/4, c = lane%4) holds
 // A elements (rows g and g+8) and B elements (code g) at k slots {2c, 2c+1,
 // 2c+8, 2c+9}.  A dot product does not care which physical k feeds which slot
@@ -174,6 +191,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1) restricted_head_kernel(const Re
     // this lane's code for the reduction below, loaded with the operands
     const int t_lane = u0 + lane < U ? a.union_ids[u0 + lane] : -1;
     const uint4* Wv = reinterpret_cast<const uint4*>(a.W);
+    const uint64_t pol_w = l2_evict_last_policy();   // the union's rows stay in L2 for the next call
     const bool tiled = a.w_tiled != 0;
     size_t wb[4];
 #pragma unroll
@@ -196,7 +214,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1) restricted_head_kernel(const Re
           A0[j] = hA[v];
           A1[j] = hB[v];
 #pragma unroll
-          for (int nt = 0; nt < 4; ++nt) B[j][nt] = Wv[w_vec(wb[nt], v + c, tiled)];
+          for (int nt = 0; nt < 4; ++nt) B[j][nt] = ld_keep_l2(Wv + w_vec(wb[nt], v + c, tiled), pol_w);
         }
       }
 #pragma unroll
