@@ -1,0 +1,74 @@
+"""Seeded random configurations against the oracle: hidden sizes, vocabulary
+sizes (ragged against the 256-column tiles), set counts and sizes, candidate
+lengths, kinds, duplicate rates, temperatures and row layouts in full mode;
+unions of 1 to 150 codes (one to five 32-code groups of the restricted head)
+in restricted mode.  Every case is fixed by its seed, so a failure reproduces."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as wk
+from parity import check_duplicates, compare
+from test_gpu_parity import run_gpu
+
+pytestmark = pytest.mark.gpu
+
+D_CHOICES = (64, 128, 192, 256, 512, 1024)
+T_CHOICES = (0.5, 1.0, 2.179, 5.0)
+
+
+@pytest.fixture(scope="module")
+def jet():
+    import candidate_answer_scoring_gb300 as jet
+    jet.load()
+    return jet
+
+
+def full_case(seed):
+    rng = np.random.default_rng(1000 + seed)
+    d = int(rng.choice(D_CHOICES))
+    V = int(rng.integers(50, 5000))
+    n_sets = int(rng.integers(1, 60))
+    k_hi = int(rng.integers(1, 12))
+    len_hi = int(rng.integers(1, 7))
+    kinds = tuple(int(k) for k in rng.choice(3, size=int(rng.integers(1, 4)), replace=False))
+    row_mode = "per_token" if rng.random() < 0.6 else "per_key"
+    peak = (0.3, 0.9) if rng.random() < 0.4 else None
+    return wk.custom(d, V, n_sets, K=(1, max(1, k_hi)), length=(1, len_hi), kinds=kinds, row_mode=row_mode,
+                     peak=peak, dup_prob=float(rng.uniform(0, 0.4)), T=float(rng.choice(T_CHOICES)),
+                     seed=5000 + seed)
+
+
+def restricted_case(seed):
+    rng = np.random.default_rng(2000 + seed)
+    d = int(rng.choice(D_CHOICES))
+    V = int(rng.integers(200, 6000))
+    n_union = int(rng.integers(1, 151))
+    union = rng.choice(V, size=n_union, replace=False).astype(np.int32)
+    sets = []
+    for _ in range(int(rng.integers(1, 50))):
+        K = int(rng.integers(1, min(n_union, 10) + 1))
+        codes = rng.choice(union, size=K, replace=False)
+        if K > 1 and rng.random() < 0.3:
+            codes[-1] = codes[0]                    # a duplicated code within the set
+        sets.append(wk._SetSpec(wk.KIND_CHOICE, [(int(t),) for t in codes]))
+    T = float(rng.choice(T_CHOICES))
+    W = wk.gen_W(7000 + seed, V, d)
+    wl = wk._build(f"fuzz-restricted-{seed}", 7000 + seed, d, V, W, sets, T, row_mode="per_key")
+    return wl.with_mode(wk.MODE_RESTRICTED, T, union)
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_fuzz_full(jet, seed):
+    wl = full_case(seed)
+    gpu = run_gpu(jet, wl)
+    compare(wl, gpu, oracle.score_workload(wl))
+    check_duplicates(wl, gpu)
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_fuzz_restricted(jet, seed):
+    wl = restricted_case(seed)
+    gpu = run_gpu(jet, wl)
+    compare(wl, gpu, oracle.score_workload(wl))
+    check_duplicates(wl, gpu)
