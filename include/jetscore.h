@@ -239,7 +239,8 @@ int jet_score_sets_host(jet_ctx *ctx, const void *H_bf16_host, const void *W_bf1
  * token's row is remapped so that scoring (H_unique, tok_row_unique) gives the
  * same results as scoring (H, tok_row).  Rows are compared by content (a
  * 64-bit hash, confirmed byte by byte), so different rows are never merged.
- *   H [n_rows, d] bf16 (device, 16-byte aligned); tok_row [n_tok] int32.
+ *   H [n_rows, d] bf16 (device, 16-byte aligned); tok_row [n_tok] int32
+ *     (n_tok may be 0: the rows are compacted and no token is remapped).
  *   H_unique [n_rows, d] bf16 (device, caller-owned, must not overlap H):
  *     rows 0 .. *n_unique-1 are written.
  *   tok_row_unique [n_tok] int32 (device): row of each token in H_unique.
