@@ -249,7 +249,9 @@ def reference_arm(args, world, rank):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": k_run, "steps_requested": K, "warmup": W, "ms_per_step": 1e3 * el / k_run,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOADS[name][3]},
+        "config": {"workload": WORKLOADS[name][3], "d": wl.d, "V": wl.V, "N": wl.N, "n_tok": wl.n_tok,
+                   "n_cand": wl.n_cand, "n_sets": wl.n_sets, "modes": list(WORKLOADS[name][1]),
+                   "parallelism": "rank 0 (host cores)", "accumulate": "fp64 (oracle)"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
