@@ -423,7 +423,11 @@ def gpu_arm(args, world, rank, local):
         },
         "gpu_launches": int(launches),
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                     "frac": achieved / peak, "traffic": committed_traffic(name),
+                     "frac": achieved / peak,
+                     # the committed capture is of the default launch (all rows, row-major
+                     # problem rows, tiled W); other configurations report none
+                     "traffic": committed_traffic(name) if not (args.dedup or args.gather_rows
+                                                                or args.w_layout != "tiled") else None,
                      "kernel": "head_lse_gather (tcgen05)", "kernel_ms": head_ms,
                      "algorithmic_bytes": bytes_, "algorithmic_flops": flops,
                      "t_tensor_us_sustained": t_tc * 1e6, "t_tensor_us_burst": t_tc_burst * 1e6,
