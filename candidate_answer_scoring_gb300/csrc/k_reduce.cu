@@ -12,17 +12,12 @@ namespace {
 // ---------------------------------------------------------------------------
 // lse[r] = M + log sum_i s_i exp(m_i - M) over the 2*S partials of row r
 // ("JET: Justification Evaluation in Transformer", Eq. 2).  One warp per row:
-// lane l folds partials l, l+32, ... into a running (max, sum), and the lanes
-// combine in a fixed butterfly, so identical rows give bit-identical results.
+// lane l folds partials l, l+32, ... into a running (max, sum), then the
+// lanes take the row's maximum and sum their rescaled sums, both in a fixed
+// butterfly, so identical rows give bit-identical results.
 // With sets, the row's lse goes to lse_row and the set kernel forms each
 // token's logp = z - lse; without (one token per row), logp[r] is written here.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void lse_fold(float& m, float& s, float m2, float s2) {
-  const float mn = fmaxf(m, m2);
-  if (mn == -INFINITY) return;                       // both empty
-  s = s * expf(m - mn) + s2 * expf(m2 - mn);
-  m = mn;
-}
 
 constexpr int MERGE_LOADS = 8;
 
@@ -50,17 +45,28 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeArgs a) {
       p[i] = sl < n_slots ? a.part[part_slot(P, plan_unit_of(P, m_tile, sl >> 1), sub, sl & 1, lr)]
                           : make_float2(-INFINITY, 0.f);
     }
+    // the round's maximum first, then its terms scaled to it: independent
+    // exponentials instead of a chain of pairwise folds
+    float mr = m;
 #pragma unroll
-    for (int i = 0; i < MERGE_LOADS; ++i) lse_fold(m, s, p[i].x, p[i].y);
-  }
+    for (int i = 0; i < MERGE_LOADS; ++i) mr = fmaxf(mr, p[i].x);
+    if (mr != -INFINITY) {
+      float acc = m == -INFINITY ? 0.f : s * expf(m - mr);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-    lse_fold(m, s, m2, s2);
+      for (int i = 0; i < MERGE_LOADS; ++i) acc += p[i].x == -INFINITY ? 0.f : p[i].y * expf(p[i].x - mr);
+      s = acc;
+      m = mr;
+    }
   }
+  // the row's maximum over the lanes, then the lanes' sums rescaled to it
+  float M = m;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float S = m == -INFINITY ? 0.f : s * expf(m - M);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
   if (err != 0 || lane != 0) return;
-  const float lse = m + logf(s);
+  const float lse = M + logf(S);
   if (a.lse) a.lse[r] = lse;
   if (a.lse_row) a.lse_row[r] = lse;
   else a.logp[r] = a.zg[r] - lse;
