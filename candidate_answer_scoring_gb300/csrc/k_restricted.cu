@@ -31,7 +31,9 @@
 //  2. restricted_sets_kernel, one warp per set: checks the set's offsets and
 //     kind, that each candidate is one token whose id and row are in range and
 //     whose id the map places in the union (the map is trusted only where
-//     union_ids agrees, so stale entries from earlier calls are harmless),
+//     union_ids agrees, so stale entries from earlier calls are harmless;
+//     with at most 32 codes the warp instead finds each token's position in
+//     union_ids itself, before the wait),
 //     forms logp, then runs the set rules.  Warp 0 of CTA 0 checks the ends of
 //     the offset arrays and that the union ids are in range and distinct.
 #include <cuda_bf16.h>
@@ -366,6 +368,18 @@ __global__ void __launch_bounds__(32 * RS_WARPS) restricted_sets_kernel(const Re
       }
     }
   }
+  // unions of up to 32 codes: each candidate's union position from union_ids
+  // itself (a caller input), so only the logit load waits for the head
+  const bool pos_early = live && set_code == 0 && ra.zu && c1 - c0 <= 32 && U <= 32;
+  int pos_pre = -1;
+  if (pos_early) {
+    const int u_lane = lane < U ? ra.union_ids[lane] : -1;
+    const bool mine = lane < c1 - c0 && cand_code == 0;
+    for (int j = 0; j < U; ++j) {
+      const int uj = __shfl_sync(0xffffffffu, u_lane, j);
+      if (mine && pos_pre < 0 && uj == tok) pos_pre = j;   // first position (a repeat is reported below)
+    }
+  }
   pdl_wait();
   pdl_trigger();
   if (ra.row_index)   // gathered rows: every index within the source array
@@ -401,13 +415,13 @@ __global__ void __launch_bounds__(32 * RS_WARPS) restricted_sets_kernel(const Re
         set_error(err, cand_code, cand_at);
         bad = true;
       } else {
-        const int pos = ra.umap[tok];
+        const int pos = pos_early ? pos_pre : ra.umap[tok];
         const float lse = ra.lse_row[row];
         if (pos < 0 || pos >= U) {
           set_error(err, JET_ERR_NOT_IN_UNION, t0);
           bad = true;
         } else {
-          const int uid = ra.union_ids[pos];
+          const int uid = pos_early ? tok : ra.union_ids[pos];   // found by id: no stale entry
           const float z = ra.zu[(size_t)row * U + pos];
           if (uid != tok) {   // a stale map entry
             set_error(err, JET_ERR_NOT_IN_UNION, t0);
