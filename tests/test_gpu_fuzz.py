@@ -72,3 +72,53 @@ def test_fuzz_restricted(jet, seed):
     gpu = run_gpu(jet, wl)
     compare(wl, gpu, oracle.score_workload(wl))
     check_duplicates(wl, gpu)
+
+
+def _dev(a):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_fuzz_score_tokens(jet, seed):
+    """jet_score_tokens (one token per row) on random shapes against the oracle's
+    per-token log-probabilities and row log-sum-exps."""
+    import torch
+    rng = np.random.default_rng(3000 + seed)
+    d = int(rng.choice(D_CHOICES))
+    V = int(rng.integers(20, 6000))
+    n = int(rng.integers(1, 700))
+    W = wk.gen_W(8000 + seed, V, d)
+    H = wk.to_bf16_bits((rng.normal(size=(n, d)) * rng.uniform(0.5, 3.0)).astype(np.float32))
+    tok = rng.integers(0, V, size=n).astype(np.int32)
+    sc = jet.JetScorer(d, V, n, n)
+    logp, lse = sc.score_tokens(_dev(H.view(np.int16)).view(torch.bfloat16), _dev(W.view(np.int16)).view(torch.bfloat16),
+                                _dev(tok), want_lse=True)
+    torch.cuda.synchronize()
+    ref_lp, ref_lse = oracle.score_tokens(H, W, np.arange(n, dtype=np.int32), tok)
+    assert np.abs(logp.cpu().numpy() - ref_lp).max() <= 2e-3
+    assert np.abs(lse.cpu().numpy() - ref_lse).max() <= 2e-3
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_fuzz_gather_rows(jet, seed):
+    """jet_score_sets_gather: the problem rows scattered at random positions of a
+    larger source array (padding rows between them hold other values); results
+    equal the compact call's bit for bit, full or restricted."""
+    import torch
+    restricted = seed % 3 == 2
+    wl = restricted_case(seed) if restricted else full_case(100 + seed)
+    rng = np.random.default_rng(4000 + seed)
+    n_src = wl.N + int(rng.integers(0, 3 * wl.N + 2))
+    pos = np.sort(rng.choice(n_src, size=wl.N, replace=False)).astype(np.int32)
+    src = wk.to_bf16_bits(rng.normal(size=(n_src, wl.d)).astype(np.float32))
+    src[pos] = wl.H
+    sc = jet.JetScorer(wl.d, wl.V, wl.N, wl.n_tok)
+    W = _dev(wl.W.view(np.int16)).view(torch.bfloat16)
+    rest = (_dev(wl.tok_row), _dev(wl.tok_ids), _dev(wl.cand_offsets), _dev(wl.set_offsets), _dev(wl.kind), wl.T,
+            wl.mode, None if wl.union_ids is None else _dev(wl.union_ids))
+    got = sc.score_sets_gather(_dev(src.view(np.int16)).view(torch.bfloat16), _dev(pos), W, *rest)
+    got = {k: v.cpu().numpy() for k, v in got.items()}
+    compact = sc.score_sets(_dev(wl.H.view(np.int16)).view(torch.bfloat16), W, *rest)
+    for k, v in compact.items():
+        assert np.array_equal(got[k].view(np.uint32), v.cpu().numpy().view(np.uint32)), k
