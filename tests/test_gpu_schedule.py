@@ -50,9 +50,15 @@ print(json.dumps(info))
 """
 
 
+def _base_env():
+    # this file tests the paired head's unit order: diagnostic overrides of the
+    # head variant or the order set for the whole suite do not apply here
+    return {k: v for k, v in os.environ.items() if k not in ("JETSCORE_HEAD_PAIR", "JETSCORE_HEAD_DYN")}
+
+
 def _run(env, path):
     code = SCRIPT.format(root=ROOT, wl_args=WL_ARGS, out=path)
-    r = subprocess.run([sys.executable, "-c", code], env={**os.environ, **env}, capture_output=True, text=True,
+    r = subprocess.run([sys.executable, "-c", code], env={**_base_env(), **env}, capture_output=True, text=True,
                        timeout=900)
     assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-4000:]
     import json
@@ -113,6 +119,6 @@ def test_many_waves_rejected_batch_stops_promptly_and_context_recovers():
     (no bounded wait runs out), and the next valid call on the same context
     reproduces the earlier outputs bit for bit."""
     code = ERR_SCRIPT.format(root=ROOT, wl_args=WL_ARGS)
-    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=900)
+    r = subprocess.run([sys.executable, "-c", code], env=_base_env(), capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-4000:]
     assert r.stdout.strip().startswith("ok"), r.stdout
