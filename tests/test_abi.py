@@ -52,3 +52,42 @@ def test_product_path_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(js, "library_path", lambda: str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         js.load()
+
+
+C_PROGRAM = r"""
+#include <stdio.h>
+#include <string.h>
+#include "jetscore.h"
+
+int main(void) {
+  jet_ctx *ctx = NULL;
+  jet_set_out out;
+  memset(&out, 0, sizeof out);
+  /* host checks run before any CUDA call: no device needed */
+  if (jet_create(&ctx, 63, 1000, 16, 16, 0) != JET_ERR_ARG) return 1;      /* d % 64 != 0 */
+  if (jet_score_sets(NULL, NULL, NULL, 1, NULL, NULL, 1, NULL, 1, NULL, NULL, 1, 1.0f,
+                     JET_MODE_FULL, NULL, 0, &out, NULL) != JET_ERR_ARG) return 2;
+  if (strcmp(jet_status_string(JET_OK), "ok") != 0) return 3;
+  printf("%s|%s\n", jet_status_string(JET_ERR_TOKEN_RANGE), jet_status_string(JET_ERR_TIMEOUT));
+  return 0;
+}
+"""
+
+
+@pytest.mark.skipif(shutil.which("gcc") is None, reason="no C compiler")
+def test_header_compiles_as_c99_and_links_from_c(tmp_path):
+    """include/jetscore.h is plain C (C99, -pedantic, warnings as errors) and a
+    C program links against libjetscore.so and runs its host-side checks."""
+    import subprocess
+    from candidate_answer_scoring_gb300 import build
+    lib = build.build()
+    src = tmp_path / "use_abi.c"
+    src.write_text(C_PROGRAM)
+    exe = tmp_path / "use_abi"
+    libdir = os.path.dirname(lib)
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", f"-I{ROOT}/include", str(src),
+                    f"-L{libdir}", "-l:" + os.path.basename(lib), f"-Wl,-rpath,{libdir}", "-o", str(exe)],
+                   check=True, capture_output=True, text=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, (r.returncode, r.stdout, r.stderr)
+    assert r.stdout.strip() == "token id or row index out of range|device-side wait timed out"
