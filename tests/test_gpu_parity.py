@@ -441,3 +441,29 @@ def test_full_size_against_stored_oracle_sets(jet, name):
     orc.decision = np.asarray(g["decision"], np.int32)
     compare(wl, gpu, orc, np.asarray(g["sets"]), np.asarray(g["cands"]), np.asarray(g["tokens"]),
             np.asarray(g["rows"]))
+
+
+def test_two_contexts_on_two_streams_run_concurrently(jet):
+    """Contexts share no device state: a full-vocabulary batch on one stream
+    and a restricted batch on another, enqueued alternately without waiting,
+    give the same bits as each run alone."""
+    full = wk.custom(128, 2600, 50, K=(2, 8), length=(1, 5), seed=61)
+    rest = wk.binary_restricted(base=wk.binary_batch(n_questions=300, random_pairs=True, d=128, V=2600))
+    jobs = []
+    for wl in (full, rest):
+        sc = jet.JetScorer(wl.d, wl.V, wl.N, wl.n_tok)
+        x = to_dev(wl)
+        alone = run_gpu(jet, wl, sc, x)
+        jobs.append((wl, sc, x, alone, torch.cuda.Stream()))
+    outs = [None, None]
+    for _ in range(5):
+        for i, (wl, sc, x, alone, st) in enumerate(jobs):
+            with torch.cuda.stream(st):
+                outs[i] = sc.score_sets(x["H"], x["W"], x["tok_row"], x["tok_ids"], x["cand_offsets"],
+                                        x["set_offsets"], x["kind"], wl.T, wl.mode, x.get("union_ids"), sync=False)
+    torch.cuda.synchronize()
+    for (wl, sc, x, alone, st), out in zip(jobs, outs):
+        assert sc.sync_status() == 0
+        for k in OUT_KEYS:
+            got = out[k].cpu().numpy()
+            assert np.array_equal(got.view(np.uint32), alone[k].view(np.uint32)), (wl.name, k)
