@@ -467,3 +467,42 @@ def test_two_contexts_on_two_streams_run_concurrently(jet):
         for k in OUT_KEYS:
             got = out[k].cpu().numpy()
             assert np.array_equal(got.view(np.uint32), alone[k].view(np.uint32)), (wl.name, k)
+
+
+def test_async_calls_capture_into_a_cuda_graph(jet):
+    """score_sets(sync=False) records into a CUDA graph (host checks and
+    tensor-map encoding happen at capture; every launch is a graph node), and
+    each replay reproduces the stream-launched results bit for bit, full and
+    restricted mode in one graph."""
+    full = wk.custom(128, 2600, 40, K=(2, 8), length=(1, 5), seed=71)
+    rest = wk.binary_restricted(base=wk.binary_batch(n_questions=100, random_pairs=True, d=128, V=2600))
+    sc = jet.JetScorer(128, 2600, max(full.N, rest.N), max(full.n_tok, rest.n_tok))
+    xs = [to_dev(full), to_dev(rest)]
+    wls = [full, rest]
+    outs = [sc.alloc_outputs(w.N, w.n_tok, w.n_cand, w.n_sets) for w in wls]
+    st = torch.cuda.Stream()
+
+    def step():
+        for w, x, o in zip(wls, xs, outs):
+            sc.score_sets(x["H"], x["W"], x["tok_row"], x["tok_ids"], x["cand_offsets"], x["set_offsets"],
+                          x["kind"], w.T, w.mode, x["union_ids"], out=o, sync=False)
+
+    with torch.cuda.stream(st):
+        step()
+    torch.cuda.synchronize()
+    ref = [{k: v.clone() for k, v in o.items()} for o in outs]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st):
+        step()
+    for _ in range(2):
+        for o in outs:
+            for v in o.values():
+                v.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert sc.sync_status() == 0
+        for o, r in zip(outs, ref):
+            for k in o:
+                assert torch.equal(o[k], r[k]), k
+    for w, o in zip(wls, outs):
+        compare(w, {k: v.cpu().numpy() for k, v in o.items()}, oracle.score_workload(w))
