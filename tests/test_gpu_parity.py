@@ -195,7 +195,7 @@ def test_edge_cases(jet):
     compare(wl, gpu, oracle.score_workload(wl))
 
 
-@pytest.mark.parametrize("case", ["vocab-below-one-tile", "widest-rows", "single-code-union"])
+@pytest.mark.parametrize("case", ["vocab-below-one-tile", "widest-rows", "single-code-union", "million-vocab"])
 def test_shape_extremes(jet, case):
     """A vocabulary smaller than one 256-column tile (every column ragged), the
     widest rows the library accepts (d = 16384: 256 k-blocks per tile) through
@@ -206,6 +206,13 @@ def test_shape_extremes(jet, case):
     elif case == "widest-rows":
         wls = [wk.custom(16384, 700, 4, K=(2, 4), length=(1, 2), seed=92),      # N <= 128: one-CTA head
                wk.binary_batch(150, random_pairs=True, d=16384, V=600)]          # N > 128: paired head
+    elif case == "million-vocab":     # 4097 vocabulary tiles, the last ragged; ids near the top of the range
+        V = 1048583
+        wls = [wk.custom(64, V, 8, K=(2, 5), length=(1, 3), seed=94),                  # one-CTA head
+               wk.binary_batch(140, random_pairs=True, d=64, V=V)]                     # paired head
+        top = np.arange(V - 40, V, dtype=np.int32)
+        rest = wk.binary_batch(30, random_pairs=True, d=64, V=V)
+        wls.append(rest.with_mode(wk.MODE_RESTRICTED, 2.179, np.unique(np.concatenate([rest.tok_ids, top]))))
     else:
         base = wk.custom(64, 400, 5, K=(1, 1), length=(1, 1), kinds=(0,), seed=93)
         wls = [base.with_mode(wk.MODE_RESTRICTED, 1.0, np.unique(base.tok_ids)[:1])]
