@@ -93,3 +93,28 @@ def test_tiled_weights_reject_bad_arguments(jet):
     p = C.c_void_p(W.data_ptr())
     assert sc.lib.jet_tile_weights(sc._h, p, p, None) == -1         # the tiled copy may not overlap W
     assert sc.lib.jet_tile_weights(sc._h, None, p, None) == -1
+
+
+def test_tiled_weights_in_score_tokens_and_many_waves(jet):
+    """The per-position entry, and a paired head running several waves of units
+    in counter order, read the tiled copy with the same bits as row-major W."""
+    import torch
+    rng = np.random.default_rng(37)
+    d, V, n = 128, 3000, 22000           # 86 paired row tiles, more than the 76 pairs: several waves
+    W = wk.gen_W(3737, V, d)
+    H = wk.to_bf16_bits(rng.normal(size=(n, d)).astype(np.float32))
+    tok = rng.integers(0, V, size=n).astype(np.int32)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    Wd = dev(W.view(np.int16)).view(torch.bfloat16)
+    Hd = dev(H.view(np.int16)).view(torch.bfloat16)
+    sc = jet.JetScorer(d, V, n, n)
+    info = sc.plan_info(n)
+    assert info["tile_rows"] == 256 and info["units"] > info["ctas"] // 2, info
+    lp_row, lse_row = sc.score_tokens(Hd, Wd, dev(tok), want_lse=True)
+    Wt = sc.tile_weights(Wd)
+    lp_t, lse_t = sc.score_tokens(Hd, Wt, dev(tok), want_lse=True)
+    torch.cuda.synchronize()
+    assert torch.equal(lp_row, lp_t) and torch.equal(lse_row, lse_t)
+    ref_lp, ref_lse = oracle.score_tokens(H, W, np.arange(n, dtype=np.int32), tok)
+    assert np.abs(lp_t.cpu().numpy() - ref_lp).max() <= 2e-3
+    assert np.abs(lse_t.cpu().numpy() - ref_lse).max() <= 2e-3
