@@ -11,7 +11,8 @@
 //
 // Structure (persistent CTAs, 320 threads each):
 //   warp 0      TMA producer: H and W k-blocks (64 bf16 = 128 B, 128B swizzle)
-//               into a shared-memory ring, completion on mbarriers;
+//               into a shared-memory ring of stages of two k-blocks each,
+//               completion on mbarriers;
 //   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators) and
 //               issues tcgen05.mma (K=16 per instruction) from one thread;
 //   warps 2-9   epilogue: each thread owns one row (its TMEM lane) and half of
@@ -23,8 +24,8 @@
 //
 // Paired variant (PAIR = true, clusters of two CTAs on two SMs): one
 // tcgen05.mma.cta_group::2 computes a 256 x 256 tile; each CTA stages its own
-// 128 rows of H and 128 of the tile's 256 W rows, so its 6-stage ring holds
-// twice the W bytes of the single-CTA ring.  This is what lets few rows
+// 128 rows of H and 128 of the tile's 256 W rows, so its 3-stage ring
+// (6 k-blocks) holds twice the W bytes of the single-CTA ring.  This is what lets few rows
 // (N ~ 256, where two row tiles would otherwise share each W tile and halve
 // each CTA's DRAM bytes in flight) stream W at full bandwidth.  Both CTAs'
 // TMA copies complete on the issuing CTA's barrier, which expects the bytes of
@@ -455,19 +456,27 @@ __global__ void __launch_bounds__(HEAD_THREADS, 1)
         for (int vt = vt0; ok && vt < vt1; ++vt) {
           if (*abort_flag) { ok = false; break; }
           const int b_row = vt * BN + (int)rank * SH::B_ROWS;
-          for (int kb = 0; kb < kblocks; ++kb) {
+          for (int kb = 0; kb < kblocks; kb += SH::KPS) {
+            const int nk = min(SH::KPS, kblocks - kb);   // k-blocks in this stage (the last may be short)
+            const uint32_t bytes = (uint32_t)nk * (SH::A_KB_BYTES + SH::B_KB_BYTES);
             if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.err, 1, WAIT_LIMIT_NS)) { ok = false; break; }
+            uint8_t* dA = sA + stage * SH::A_BYTES;
+            uint8_t* dB = sB + stage * SH::B_BYTES;
             if constexpr (PAIR) {
-              if (issuer) mbar_arrive_expect_tx(&full[stage], 2 * SH::STAGE_BYTES);   // both CTAs' halves
+              if (issuer) mbar_arrive_expect_tx(&full[stage], 2 * bytes);   // both CTAs' halves
               const uint32_t bar = cluster_addr(&full[stage], 0);
-              tma_load_2d_pair(sA + stage * SH::A_BYTES, &tmH, kb * BK, a_row, bar, pol_h);
-              if (a.w_tiled) tma_load_4d_pair(sB + stage * SH::B_BYTES, &tmW, kb, b_row >> 7, bar, pol_w);
-              else tma_load_2d_pair(sB + stage * SH::B_BYTES, &tmW, kb * BK, b_row, bar, pol_w);
+              for (int j = 0; j < nk; ++j) {
+                tma_load_2d_pair(dA + j * SH::A_KB_BYTES, &tmH, (kb + j) * BK, a_row, bar, pol_h);
+                if (a.w_tiled) tma_load_4d_pair(dB + j * SH::B_KB_BYTES, &tmW, kb + j, b_row >> 7, bar, pol_w);
+                else tma_load_2d_pair(dB + j * SH::B_KB_BYTES, &tmW, (kb + j) * BK, b_row, bar, pol_w);
+              }
             } else {
-              mbar_arrive_expect_tx(&full[stage], SH::STAGE_BYTES);
-              tma_load_2d(sA + stage * SH::A_BYTES, &tmH, kb * BK, a_row, &full[stage], pol_h);
-              if (a.w_tiled) tma_load_4d(sB + stage * SH::B_BYTES, &tmW, kb, b_row >> 7, &full[stage], pol_w);
-              else tma_load_2d(sB + stage * SH::B_BYTES, &tmW, kb * BK, b_row, &full[stage], pol_w);
+              mbar_arrive_expect_tx(&full[stage], bytes);
+              for (int j = 0; j < nk; ++j) {
+                tma_load_2d(dA + j * SH::A_KB_BYTES, &tmH, (kb + j) * BK, a_row, &full[stage], pol_h);
+                if (a.w_tiled) tma_load_4d(dB + j * SH::B_KB_BYTES, &tmW, kb + j, b_row >> 7, &full[stage], pol_w);
+                else tma_load_2d(dB + j * SH::B_KB_BYTES, &tmW, (kb + j) * BK, b_row, &full[stage], pol_w);
+              }
             }
             if (a.pf_kblocks > 0 && !a.w_tiled) {   // optional: more W bytes in flight than the ring holds
               const int ip = (vt - vt0) * kblocks + kb + a.pf_kblocks;
@@ -527,14 +536,20 @@ __global__ void __launch_bounds__(HEAD_THREADS, 1)
           if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, a.err, 2, WAIT_LIMIT_NS)) { ok = false; break; }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-          for (int kb = 0; kb < kblocks; ++kb) {
+          for (int kb = 0; kb < kblocks; kb += SH::KPS) {
+            const int nk = min(SH::KPS, kblocks - kb);
             if (!mbar_wait(&full[stage], phase, abort_flag, a.err, 3, WAIT_LIMIT_NS)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t a0 = smem_u32(sA + stage * SH::A_BYTES);
-            const uint32_t b0 = smem_u32(sB + stage * SH::B_BYTES);
 #pragma unroll
-            for (int k = 0; k < BK / 16; ++k)   // 16 bf16 = 32 bytes along K per MMA
-              tc_mma<PAIR>(d_tmem, sdesc_k128(a0 + 32 * k), sdesc_k128(b0 + 32 * k), (kb | k) != 0);
+            for (int j = 0; j < SH::KPS; ++j) {
+              if (j < nk) {
+                const uint32_t a0 = smem_u32(sA + stage * SH::A_BYTES + j * SH::A_KB_BYTES);
+                const uint32_t b0 = smem_u32(sB + stage * SH::B_BYTES + j * SH::B_KB_BYTES);
+#pragma unroll
+                for (int k = 0; k < BK / 16; ++k)   // 16 bf16 = 32 bytes along K per MMA
+                  tc_mma<PAIR>(d_tmem, sdesc_k128(a0 + 32 * k), sdesc_k128(b0 + 32 * k), (kb | j | k) != 0);
+              }
+            }
             tc_commit_all<PAIR>(&empty[stage]);
             any = true;
             if (++stage == NST) { stage = 0; phase ^= 1u; }
