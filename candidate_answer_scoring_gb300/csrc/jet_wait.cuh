@@ -48,9 +48,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Bounded wait for the phase of `bar` with the given parity.  Returns false if
 // another role raised *abort_flag or if the wait exceeded limit_ns (then it
 // raises the flag itself and, when err is given, records JET_ERR_TIMEOUT and
-// `where` in err[2]).
-__device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err,
-                                       int where, unsigned long long limit_ns) {
+// `where` in err[2]).  The spinning part is out of line; mbar_wait below
+// tries the barrier once inline first.
+__device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err,
+                                            int where, unsigned long long limit_ns) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const unsigned long long t0 = globaltimer();
@@ -65,6 +66,15 @@ __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile 
       }
     }
   }
+}
+
+// A phase that has already completed (the common case for the MMA thread
+// and the producer) costs one try_wait and no call (measured: multitoken
+// head 2% faster than with the call on every wait).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err,
+                                          int where, unsigned long long limit_ns) {
+  if (mbar_try_wait(smem_u32(bar), parity)) return true;
+  return mbar_wait_slow(bar, parity, abort_flag, err, where, limit_ns);
 }
 
 }  // namespace
