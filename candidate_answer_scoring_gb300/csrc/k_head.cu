@@ -11,8 +11,9 @@
 //
 // Structure (persistent CTAs, 320 threads each):
 //   warp 0      TMA producer: H and W k-blocks (64 bf16 = 128 B, 128B swizzle)
-//               into a shared-memory ring of stages of two k-blocks each,
-//               completion on mbarriers;
+//               into a shared-memory ring (stages of two k-blocks for the
+//               paired head, one for the one-CTA head), completion on
+//               mbarriers;
 //   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators) and
 //               issues tcgen05.mma (K=16 per instruction) from one thread;
 //   warps 2-9   epilogue: each thread owns one row (its TMEM lane) and half of
