@@ -24,22 +24,23 @@ constexpr int EPI_WARPS = 8;        // two warpgroups: column halves of a tile
 constexpr int HEAD_THREADS = (2 + EPI_WARPS) * 32;
 constexpr int TMEM_COLS = 2 * BN;   // two accumulators (double buffer)
 
-// A ring stage holds KPS consecutive k-blocks of H and of W: the MMA thread
-// waits once and commits once per stage.  Paired: stages of two k-blocks
-// halved that thread's per-k-block overhead and made the tensor-bound heads
-// ~11% faster (3 stages, the same bytes in flight as 6 of one k-block).  One
-// CTA: a k-block is already 48 KB, and two stages of two were 4% slower than
-// four of one (128-row batches), so it keeps four.
-template <bool PAIR>
+// A ring stage holds KPS consecutive k-blocks of H and of W; the MMA thread
+// waits once and commits once per stage.  Paired head, schedules of several
+// waves of units (tensor-bound batches): stages of two k-blocks (3 stages,
+// the same bytes in flight as 6 of one), 1-2% faster there.  One wave (few
+// row tiles, W streaming): six stages of one k-block, 3% faster on the
+// 256-row batch.  One CTA: four stages of one 48 KB k-block (two of two were
+// 4% slower on 128-row batches).
+template <bool PAIR, int KPS_ = 1>
 struct HeadShape {
   static constexpr int B_ROWS = PAIR ? BN / 2 : BN;   // W rows this CTA stages per tile
-  static constexpr int KPS = PAIR ? 2 : 1;             // k-blocks per ring stage
+  static constexpr int KPS = KPS_;                     // k-blocks per ring stage
   static constexpr int A_KB_BYTES = BM * BK * 2;       // one k-block of this CTA's H rows
   static constexpr int B_KB_BYTES = B_ROWS * BK * 2;   // one k-block of this CTA's W rows
   static constexpr int A_BYTES = KPS * A_KB_BYTES;
   static constexpr int B_BYTES = KPS * B_KB_BYTES;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = PAIR ? 3 : 4;          // shared-memory ring depth
+  static constexpr int STAGES = !PAIR ? 4 : (KPS == 1 ? 6 : 3);   // shared-memory ring depth
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 512 /*barriers, unit ring*/;
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
   static_assert(A_KB_BYTES % 1024 == 0 && B_KB_BYTES % 1024 == 0, "swizzle atoms stay 1024-byte aligned");

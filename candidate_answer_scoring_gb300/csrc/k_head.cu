@@ -11,9 +11,9 @@
 //
 // Structure (persistent CTAs, 320 threads each):
 //   warp 0      TMA producer: H and W k-blocks (64 bf16 = 128 B, 128B swizzle)
-//               into a shared-memory ring (stages of two k-blocks for the
-//               paired head, one for the one-CTA head), completion on
-//               mbarriers;
+//               into a shared-memory ring (stages of two k-blocks for a
+//               paired head with several waves of units, else one),
+//               completion on mbarriers;
 //   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators) and
 //               issues tcgen05.mma (K=16 per instruction) from one thread;
 //   warps 2-9   epilogue: each thread owns one row (its TMEM lane) and half of
@@ -25,8 +25,8 @@
 //
 // Paired variant (PAIR = true, clusters of two CTAs on two SMs): one
 // tcgen05.mma.cta_group::2 computes a 256 x 256 tile; each CTA stages its own
-// 128 rows of H and 128 of the tile's 256 W rows, so its 3-stage ring
-// (6 k-blocks) holds twice the W bytes of the single-CTA ring.  This is what lets few rows
+// 128 rows of H and 128 of the tile's 256 W rows, so its ring (6 k-blocks)
+// holds twice the W bytes of the single-CTA ring.  This is what lets few rows
 // (N ~ 256, where two row tiles would otherwise share each W tile and halve
 // each CTA's DRAM bytes in flight) stream W at full bandwidth.  Both CTAs'
 // TMA copies complete on the issuing CTA's barrier, which expects the bytes of
@@ -367,11 +367,11 @@ __device__ __forceinline__ float ex2(float x) {   // hardware 2^x (MUFU), flushe
 
 constexpr float LOG2E = 1.4426950408889634f;
 
-template <bool PAIR>
+template <bool PAIR, int KPS>
 __global__ void __launch_bounds__(HEAD_THREADS, 1)
     head_lse_gather_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmW,
                            const HeadArgs a) {
-  using SH = HeadShape<PAIR>;
+  using SH = HeadShape<PAIR, KPS>;
   constexpr int NST = SH::STAGES;
   extern __shared__ uint8_t smem_raw[];
   // 128B-swizzled operand tiles must start on 1024-byte boundaries
@@ -674,7 +674,7 @@ __global__ void __launch_bounds__(HEAD_THREADS, 1)
   }
 }
 
-template <bool PAIR>
+template <bool PAIR, int KPS>
 cudaError_t launch_variant(const CUtensorMap& tmH, const CUtensorMap& tmW, const HeadArgs& a, cudaStream_t st) {
   // the shared-memory attribute belongs to the function on each device
   static std::atomic<unsigned long long> configured{0};
@@ -683,15 +683,15 @@ cudaError_t launch_variant(const CUtensorMap& tmH, const CUtensorMap& tmW, const
   if (e != cudaSuccess) return e;
   const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
   if (bit == 0 || (configured.load() & bit) == 0) {
-    e = cudaFuncSetAttribute(head_lse_gather_kernel<PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             HeadShape<PAIR>::SMEM_BYTES);
+    e = cudaFuncSetAttribute(head_lse_gather_kernel<PAIR, KPS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             HeadShape<PAIR, KPS>::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.plan.grid);
   cfg.blockDim = dim3(HEAD_THREADS);
-  cfg.dynamicSmemBytes = HeadShape<PAIR>::SMEM_BYTES;
+  cfg.dynamicSmemBytes = HeadShape<PAIR, KPS>::SMEM_BYTES;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
   int n = 0;
@@ -709,13 +709,16 @@ cudaError_t launch_variant(const CUtensorMap& tmH, const CUtensorMap& tmW, const
   }
   cfg.attrs = attr;
   cfg.numAttrs = n;
-  return cudaLaunchKernelEx(&cfg, head_lse_gather_kernel<PAIR>, tmH, tmW, a);
+  return cudaLaunchKernelEx(&cfg, head_lse_gather_kernel<PAIR, KPS>, tmH, tmW, a);
 }
 
 }  // namespace
 
 cudaError_t launch_head(const CUtensorMap& tmH, const CUtensorMap& tmW, const HeadArgs& a, cudaStream_t st) {
-  return a.plan.pair ? launch_variant<true>(tmH, tmW, a, st) : launch_variant<false>(tmH, tmW, a, st);
+  if (!a.plan.pair) return launch_variant<false, 1>(tmH, tmW, a, st);
+  // several waves of units (more units than pairs): stages of two k-blocks
+  return a.plan.units > a.plan.grid / 2 ? launch_variant<true, 2>(tmH, tmW, a, st)
+                                        : launch_variant<true, 1>(tmH, tmW, a, st);
 }
 
 }  // namespace jet

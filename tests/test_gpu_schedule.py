@@ -122,3 +122,27 @@ def test_many_waves_rejected_batch_stops_promptly_and_context_recovers():
     r = subprocess.run([sys.executable, "-c", code], env=_base_env(), capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-4000:]
     assert r.stdout.strip().startswith("ok"), r.stdout
+
+
+def test_many_waves_with_an_odd_number_of_k_blocks():
+    """A schedule of several waves takes ring stages of two k-blocks; with
+    d = 192 (three k-blocks) every tile ends on a stage of one.  Per-position
+    scoring of 22k rows against the oracle."""
+    import torch
+    import oracle
+    import candidate_answer_scoring_gb300 as jet_mod
+    rng = np.random.default_rng(43)
+    d, V, n = 192, 1500, 22000
+    W = wk.gen_W(4343, V, d)
+    H = wk.to_bf16_bits(rng.normal(size=(n, d)).astype(np.float32))
+    tok = rng.integers(0, V, size=n).astype(np.int32)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    sc = jet_mod.JetScorer(d, V, n, n)
+    info = sc.plan_info(n)
+    assert info["tile_rows"] == 256 and info["units"] > info["ctas"] // 2, info
+    lp, lse = sc.score_tokens(dev(H.view(np.int16)).view(torch.bfloat16), dev(W.view(np.int16)).view(torch.bfloat16),
+                              dev(tok), want_lse=True)
+    torch.cuda.synchronize()
+    ref_lp, ref_lse = oracle.score_tokens(H, W, np.arange(n, dtype=np.int32), tok)
+    assert np.abs(lp.cpu().numpy() - ref_lp).max() <= 2e-3
+    assert np.abs(lse.cpu().numpy() - ref_lse).max() <= 2e-3
