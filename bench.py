@@ -1,20 +1,23 @@
 #!/usr/bin/env python
 """Benchmark of the candidate-set scoring head on GB300.
 
-One step = one pass of the whole path over one batch: for the default workload
-(256 binary questions, d=2560, V=248320) that is the full-vocabulary pass
-(pre-pass, tcgen05 head, split merge, set rules) followed by the restricted
-26-code pass (pre-pass, restricted head, set rules).  The metric is scored
-candidate tokens per second of the full-vocabulary pass (512 per step); the
-step time includes the restricted pass.
+One step = one pass of the whole path over one batch.  The headline workload
+(default) is the large batch: 16 requests x 64 candidates of 8-32 tokens,
+about 20k scored positions, d=4096, V=152064, full vocabulary: pre-pass,
+tcgen05 head, split merge, set rules.  The line's ``per_config`` block times
+the other workloads the same way: the binary batch (256 questions, d=2560,
+V=248320; full vocabulary, then the restricted 26-code pass in the same step),
+the multi-token choice batch and the wide-schema batch.  The metric is scored
+candidate tokens per second of the full-vocabulary pass.
 
 Printed: one JSON line (rank 0).  Timing: CUDA events on the launching stream,
-after warm-up, synchronised on both sides; W (1.27 GB) is larger than L2, so
+after warm-up, synchronised on both sides; W (0.8-1.3 GB) is larger than L2, so
 consecutive steps do not hit in L2 for the dominant stream.  Kernel-level
 times come from event pairs the library records around its own launches.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
-                  [--workload binary|multitoken|wideschema|large|tiny]
+                  [--workload large|binary|multitoken|wideschema|tiny]
+                  [--per-config binary,multitoken,wideschema|none]
 """
 import argparse
 import hashlib
@@ -183,24 +186,34 @@ def roofline_terms(wl, peaks, sustained, n_rows=None):
 # ---------------------------------------------------------------------------
 # CPU oracle timing (reference arm and cpu_baseline)
 # ---------------------------------------------------------------------------
-def _subset(wl, n_sets):
+def _subset(wl, n_cand):
+    """The workload cut to its first n_cand candidates (whole sets, then the
+    leading candidates of the next set, which becomes a choice set), with only
+    the hidden rows those candidates' tokens read.  The oracle's cost is one
+    full-vocabulary row per distinct row, so a candidate-granular cut keeps a
+    sample of a few hundred rows bounded even where one set holds a thousand."""
     import numpy as np
     import workloads as wk
-    k = min(n_sets, wl.n_sets)
-    c1 = int(wl.set_offsets[k])
+    c1 = max(1, min(int(n_cand), wl.n_cand))
+    so = wl.set_offsets.astype(np.int64)
+    k = int(np.searchsorted(so, c1, side="left"))      # sets [0, k) start before c1
+    set_off = np.minimum(so[:k + 1], c1).astype(np.int32)
+    set_off[k] = c1
+    kind = wl.kind[:k].copy()
+    if so[k] != c1:                                    # the last set was cut short
+        kind[k - 1] = wk.KIND_CHOICE
     t1 = int(wl.cand_offsets[c1])
     rows, new_row = np.unique(wl.tok_row[:t1], return_inverse=True)
-    return wk.Workload(wl.name + f"-first{k}", wl.d, wl.V, np.ascontiguousarray(wl.H[rows]), wl.W,
+    return wk.Workload(wl.name + f"-first{c1}c", wl.d, wl.V, np.ascontiguousarray(wl.H[rows]), wl.W,
                        new_row.astype(np.int32), wl.tok_ids[:t1].copy(), wl.cand_offsets[:c1 + 1].copy(),
-                       wl.set_offsets[:k + 1].copy(), wl.kind[:k].copy(), wl.T, wl.mode, wl.union_ids,
-                       dict(wl.info))
+                       set_off, kind, wl.T, wl.mode, wl.union_ids, dict(wl.info))
 
 
-def time_oracle(steps_wl, n_sets, repeats=1):
-    """Run the oracle on the first n_sets sets of each step workload; returns
-    (seconds per step, full-mode tokens per step, threads)."""
+def time_oracle(steps_wl, n_cand, repeats=1):
+    """Run the oracle on the first n_cand candidates of each step workload;
+    returns (seconds per step, full-mode tokens per step, threads)."""
     import oracle
-    subs = [_subset(w, n_sets) for w in steps_wl]
+    subs = [_subset(w, n_cand) for w in steps_wl]
     t0 = time.perf_counter()
     for _ in range(repeats):
         for s in subs:
@@ -209,14 +222,17 @@ def time_oracle(steps_wl, n_sets, repeats=1):
     return dt, subs[0].n_tok, oracle.max_threads()
 
 
-def cpu_sample_sets(steps_wl, n_total, target_s):
-    """Number of leading sets whose oracle run takes about target_s seconds of
-    wall time on this host (the oracle runs rows in parallel, so the probe
-    uses one set per thread)."""
+def cpu_sample_cands(steps_wl, target_s):
+    """Number of leading candidates whose oracle run takes about target_s
+    seconds of wall time on this host.  The oracle runs rows in parallel, so
+    the probe takes enough candidates for about two rows per thread."""
+    import numpy as np
     import oracle
-    probe = max(1, min(n_total, oracle.max_threads()))
+    wl = steps_wl[0]
+    rows_per_cand = max(1.0, wl.N / max(1, wl.n_cand))
+    probe = int(min(wl.n_cand, max(1, np.ceil(2 * oracle.max_threads() / rows_per_cand))))
     dt, _, _ = time_oracle(steps_wl, probe)
-    return max(1, min(n_total, int(probe * target_s / max(dt, 1e-4))))
+    return max(1, min(wl.n_cand, int(probe * target_s / max(dt, 1e-4)))), probe
 
 
 def reference_arm(args, world, rank):
@@ -227,24 +243,26 @@ def reference_arm(args, world, rank):
     import oracle
     oracle.build()
     # size one step to about 2 s of oracle work, then cap the whole run at ~3 min
-    n_sets = cpu_sample_sets(steps_wl, wl.n_sets, target_s=2.0)
+    n_cand, _ = cpu_sample_cands(steps_wl, target_s=2.0)
     K = args.steps if args.steps is not None else 5
     W = args.warmup if args.warmup is not None else 1
     budget = 180.0
     step_est = 2.0
     k_run = max(1, min(K, int(budget / max(step_est, 1e-3)) - W))
     for _ in range(W):
-        time_oracle(steps_wl, n_sets)
+        time_oracle(steps_wl, n_cand)
     t0 = time.perf_counter()
     tokens = 0
     threads = 1
     for _ in range(k_run):
-        dt, ntok, threads = time_oracle(steps_wl, n_sets)
+        dt, ntok, threads = time_oracle(steps_wl, n_cand)
         tokens += ntok
     el = time.perf_counter() - t0
     value = tokens / el
-    sample = (f"first {n_sets} of {wl.n_sets} sets per step ({_subset(wl, n_sets).n_tok} full-vocab tokens"
-              f"{' + the same sets restricted' if len(steps_wl) > 1 else ''}); fp64 C oracle, OpenMP over rows")
+    sub = _subset(wl, n_cand)
+    sample = (f"first {n_cand} of {wl.n_cand} candidates per step ({sub.n_tok} full-vocab tokens over {sub.N} "
+              f"hidden rows{', plus the same candidates restricted' if len(steps_wl) > 1 else ''}); "
+              "fp64 C oracle, OpenMP over rows")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": k_run, "steps_requested": K, "warmup": W, "ms_per_step": 1e3 * el / k_run,
@@ -262,27 +280,26 @@ def reference_arm(args, world, rank):
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
-def gpu_arm(args, world, rank, local):
+def gpu_uuid_of(dev):
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
+
+def measure_workload(name, args, dev, world, peaks, K, W, keep=False):
+    """Time K steps of one workload on the device (inputs resident, after W
+    warm-up steps), then the same K steps with the library's per-launch event
+    pairs for the kernel times.  Returns the measurements and, with keep, the
+    scorer and device inputs for the end-to-end leg."""
     import numpy as np
     import torch
 
     import candidate_answer_scoring_gb300 as jet
-    from candidate_answer_scoring_gb300 import build as libbuild
 
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    libbuild.build()
-    peaks = load_peaks()
-
-    name = args.workload
-    wl, steps_wl = make_workload(name, rank)
-    K = args.steps if args.steps is not None else WORKLOADS[name][2]
-    W = args.warmup if args.warmup is not None else 10
-    W = max(W, 3)
-
+    wl, steps_wl = make_workload(name)
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
     Wd = t(wl.W.view(np.int16)).view(torch.bfloat16)
     ins = []
@@ -290,7 +307,7 @@ def gpu_arm(args, world, rank, local):
         ins.append(dict(H=t(s.H.view(np.int16)).view(torch.bfloat16), tok_row=t(s.tok_row), tok_ids=t(s.tok_ids),
                         cand_offsets=t(s.cand_offsets), set_offsets=t(s.set_offsets), kind=t(s.kind),
                         union_ids=None if s.union_ids is None else t(s.union_ids), T=s.T, mode=s.mode, wl=s))
-    sc = jet.JetScorer(wl.d, wl.V, wl.N, wl.n_tok, device=local)
+    sc = jet.JetScorer(wl.d, wl.V, wl.N, wl.n_tok, device=dev.index)
     if args.w_layout == "tiled":
         # the output embedding is stored once in the head's tiled layout (as a
         # model loader would), outside the timed region
@@ -336,17 +353,10 @@ def gpu_arm(args, world, rank, local):
             step()
         rc = sc.sync_status()
         if rc != 0:
-            raise RuntimeError(f"device status {rc} ({jet.status_string(rc)}) after warm-up")
+            raise RuntimeError(f"{name}: device status {rc} ({jet.status_string(rc)}) after warm-up")
         torch.cuda.synchronize(dev)
 
-        gpu_uuid = None
-        try:
-            gpu_uuid = str(torch.cuda.get_device_properties(dev).uuid)
-            if not gpu_uuid.startswith("GPU-"):
-                gpu_uuid = "GPU-" + gpu_uuid
-        except Exception:
-            gpu_uuid = None
-        clocks = ClockSampler(gpu_uuid)
+        clocks = ClockSampler(gpu_uuid_of(dev))
         clocks.start()
         time.sleep(0.3)
 
@@ -377,10 +387,9 @@ def gpu_arm(args, world, rank, local):
         clk = clocks.stop()
         rc = sc.sync_status()
         if rc != 0:
-            raise RuntimeError(f"device status {rc} ({jet.status_string(rc)}) in the timed region")
+            raise RuntimeError(f"{name}: device status {rc} ({jet.status_string(rc)}) in the timed region")
     ms = max_over_ranks(ms, world, dev)
     tokens_per_step = steps_wl[0].n_tok
-    value = job_throughput(tokens_per_step, K, world, ms)
     ms_step = ms / K
 
     # kernel roofline: the full-vocabulary head
@@ -388,52 +397,95 @@ def gpu_arm(args, world, rank, local):
     head_ms = head["ms"] / max(1, head["launches"])
     flops, bytes_, t_tc, t_hbm = roofline_terms(wl, peaks, sustained=True, n_rows=n_rows_scored)
     _, _, t_tc_burst, _ = roofline_terms(wl, peaks, sustained=False, n_rows=n_rows_scored)
-    # bound by the roofline formula with the burst tensor peak; the tensor
-    # denominator is the sustained peak, since the head runs inside a long loop
+    # the bound by the roofline formula with the burst tensor peak
     bound = "hbm" if t_hbm >= t_tc_burst else "tensor"
+    tflops = flops / (head_ms / 1e3) / 1e12
+    gbs = bytes_ / (head_ms / 1e3) / 1e9
     if bound == "hbm":
-        achieved = bytes_ / (head_ms / 1e3) / 1e9
-        peak, unit = peaks["hbm"], "GB/s"
+        achieved, peak, unit = gbs, peaks["hbm"], "GB/s"
     else:
-        achieved = flops / (head_ms / 1e3) / 1e12
-        peak, unit = peaks["bf16_sustained"], "TFLOP/s"
+        # the burst peak: the head is timed in a loop well under a second
+        # long, not the seconds-long loop the sustained figure comes from
+        achieved, peak, unit = tflops, peaks["bf16"], "TFLOP/s"
     launches = sum(v["launches"] for k, v in prof.items() if isinstance(v, dict))   # = launches of pass (1)
-    t_roof = max(t_tc, t_hbm)
-
-    line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
-        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": "synthetic",
-        "config": {
-            "workload": WORKLOADS[name][3], "d": wl.d, "V": wl.V, "N": wl.N, "n_tok": wl.n_tok,
-            "n_cand": wl.n_cand, "n_sets": wl.n_sets, "modes": list(WORKLOADS[name][1]),
-            "parallelism": f"replicas x{world}",
-            "l2": "inputs larger than L2 (W = %.2f GB > 129 MB L2)" % (wl.W.nbytes / 1e9),
-            "accumulate": "fp32 (tcgen05 bf16 x bf16 -> fp32 TMEM)",
-            "plan": sc.plan_info(n_rows_scored),
-            "row_dedup": bool(args.dedup), "rows_scored": n_rows_scored,
-            "weights_layout": ("tiled (jet_tile_weights once, before timing)" if args.w_layout == "tiled"
-                               else "row-major"),
-            "row_gather": (f"rows read in place from a right-padded [N, {args.gather_rows}, d] source "
-                           "(TMA gathers)") if args.gather_rows else None,
-            "step_roofline_us": t_roof * 1e6, "step_roofline_frac": t_roof / (ms_step / 1e3),
-            "kernel_ms_per_step": {k: v["ms"] / K for k, v in prof.items() if isinstance(v, dict)},
-            "ms_per_step_with_kernel_events": ms_prof / K,
-            "peaks": peaks["source"],
-        },
-        "gpu_launches": int(launches),
+    t_roof = max(t_tc_burst, t_hbm)
+    note = "of measured" if peaks["source"] == "measured" else "of fallback"
+    rec = {
+        "name": name, "wl": wl, "steps_wl": steps_wl, "K": K, "W": W, "ms": ms, "ms_step": ms_step,
+        "value": job_throughput(tokens_per_step, K, world, ms), "tokens_per_step": tokens_per_step,
+        "n_rows_scored": n_rows_scored, "plan": sc.plan_info(n_rows_scored), "clocks": clk,
+        "gpu_launches": int(launches), "ms_prof": ms_prof, "prof": prof, "head_ms": head_ms,
+        "step_roofline_us": t_roof * 1e6, "step_roofline_frac": t_roof / (ms_step / 1e3),
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                      "frac": achieved / peak,
+                     "frac_vs_burst_tensor": t_tc_burst / (head_ms / 1e3),
+                     "frac_vs_sustained_tensor": t_tc / (head_ms / 1e3),
+                     "frac_vs_hbm": t_hbm / (head_ms / 1e3),
                      # the committed capture is of the default launch (all rows, row-major
                      # problem rows, tiled W); other configurations report none
                      "traffic": committed_traffic(name) if not (args.dedup or args.gather_rows
                                                                 or args.w_layout != "tiled") else None,
                      "kernel": "head_lse_gather (tcgen05)", "kernel_ms": head_ms,
+                     "achieved_tflops": tflops, "achieved_gbs": gbs,
                      "algorithmic_bytes": bytes_, "algorithmic_flops": flops,
                      "t_tensor_us_sustained": t_tc * 1e6, "t_tensor_us_burst": t_tc_burst * 1e6,
-                     "t_hbm_us": t_hbm * 1e6, "peak_note": "of measured" if peaks["source"] == "measured"
-                     else "of fallback"},
-        "clocks": clk,
+                     "t_hbm_us": t_hbm * 1e6, "peak_note": note},
+    }
+    if keep:
+        rec.update(sc=sc, Wd=Wd, stream=stream)
+    else:
+        sc.close()
+        del Wd, ins, outs
+        torch.cuda.synchronize(dev)
+        torch.cuda.empty_cache()
+    return rec
+
+
+def config_block(rec, args):
+    wl = rec["wl"]
+    return {"workload": WORKLOADS[rec["name"]][3], "d": wl.d, "V": wl.V, "N": wl.N, "n_tok": wl.n_tok,
+            "n_cand": wl.n_cand, "n_sets": wl.n_sets, "modes": list(WORKLOADS[rec["name"]][1]),
+            "rows_scored": rec["n_rows_scored"], "plan": rec["plan"],
+            "row_dedup": bool(args.dedup),
+            "weights_layout": ("tiled (jet_tile_weights once, before timing)" if args.w_layout == "tiled"
+                               else "row-major"),
+            "row_gather": (f"rows read in place from a right-padded [N, {args.gather_rows}, d] source "
+                           "(TMA gathers)") if args.gather_rows else None,
+            "l2": "inputs larger than L2 (W = %.2f GB > 129 MB L2)" % (wl.W.nbytes / 1e9),
+            "step_roofline_us": rec["step_roofline_us"], "step_roofline_frac": rec["step_roofline_frac"],
+            "kernel_ms_per_step": {k: v["ms"] / rec["K"] for k, v in rec["prof"].items() if isinstance(v, dict)},
+            "ms_per_step_with_kernel_events": rec["ms_prof"] / rec["K"]}
+
+
+def gpu_arm(args, world, rank, local):
+    import numpy as np
+    import torch
+
+    from candidate_answer_scoring_gb300 import build as libbuild
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    libbuild.build()
+    peaks = load_peaks()
+
+    name = args.workload
+    K = args.steps if args.steps is not None else WORKLOADS[name][2]
+    W = max(3, args.warmup if args.warmup is not None else 10)
+    rec = measure_workload(name, args, dev, world, peaks, K, W, keep=True)
+    wl, steps_wl, sc, Wd, stream = rec["wl"], rec["steps_wl"], rec["sc"], rec["Wd"], rec["stream"]
+    tokens_per_step = rec["tokens_per_step"]
+
+    cfg = config_block(rec, args)
+    cfg.update({"parallelism": f"replicas x{world}", "accumulate": "fp32 (tcgen05 bf16 x bf16 -> fp32 TMEM)",
+                "peaks": peaks["source"]})
+    line = {
+        "metric": METRIC, "value": rec["value"], "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": rec["ms_step"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic", "config": cfg, "gpu_launches": rec["gpu_launches"],
+        "roofline": rec["roofline"], "clocks": rec["clocks"],
     }
 
     # end to end through the public API with host buffers (pinned)
@@ -469,25 +521,43 @@ def gpu_arm(args, world, rank, local):
             torch.cuda.synchronize(dev)
             el = time.perf_counter() - t0
         el = max_over_ranks(el, world, dev)
-        line["e2e"] = {"value": job_throughput(tokens_per_step, Ke, world, el * 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                       "d2h_bytes_per_step": d2h, "steps": Ke, "ms_per_step": 1e3 * el / Ke,
+        line["e2e"] = {"value": job_throughput(tokens_per_step, Ke, world, el * 1e3), "unit": UNIT,
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": Ke,
+                       "ms_per_step": 1e3 * el / Ke,
                        "note": "jet_score_sets_host (the C call, arguments marshalled once) per mode: pinned host "
                                "inputs -> device -> host results; W resident on the device like any model weight"}
+    sc.close()
+    del Wd, rec
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+
+    # the other full-vocabulary workloads, each timed the same way
+    others = [w for w in (args.per_config.split(",") if args.per_config not in ("", "none") else [])
+              if w != name]
+    if others:
+        line["per_config"] = {}
+        for other in others:
+            r = measure_workload(other, args, dev, world, peaks, K, W)
+            blk = config_block(r, args)
+            blk.update({"value": r["value"], "unit": UNIT, "steps": K, "warmup": W, "ms_per_step": r["ms_step"],
+                        "head_ms": r["head_ms"], "gpu_launches": r["gpu_launches"], "roofline": r["roofline"],
+                        "clocks": r["clocks"]})
+            line["per_config"][other] = blk
 
     # CPU oracle baseline on a bounded sample (rank 0, one GPU only)
     if world == 1 and not args.no_cpu_baseline:
         import oracle
         oracle.build()
-        n_sets = cpu_sample_sets(steps_wl, wl.n_sets, target_s=15.0)
-        dt, ntok, threads = time_oracle(steps_wl, n_sets)
+        n_cand, _ = cpu_sample_cands(steps_wl, target_s=15.0)
+        dt, ntok, threads = time_oracle(steps_wl, n_cand)
+        sub = _subset(wl, n_cand)
         line["cpu_baseline"] = {
             "value": ntok / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"first {n_sets} of {wl.n_sets} sets ({ntok} full-vocab tokens"
-                      f"{', plus the restricted pass' if len(steps_wl) > 1 else ''}); {dt:.1f} s",
+            "sample": f"first {n_cand} of {wl.n_cand} candidates ({ntok} full-vocab tokens over {sub.N} hidden "
+                      f"rows{', plus the restricted pass' if len(steps_wl) > 1 else ''}); {dt:.1f} s",
         }
     if rank == 0:
         print(json.dumps(line), flush=True)
-    sc.close()
     if world > 1:
         torch.distributed.destroy_process_group()
     return 0
@@ -593,7 +663,10 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--workload", default="binary", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="large", choices=sorted(WORKLOADS),
+                    help="the headline workload (default: the large 20k-row batch, the largest)")
+    ap.add_argument("--per-config", default="binary,multitoken,wideschema",
+                    help="other workloads timed the same way into the line's per_config block ('none': skip)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--w-layout", default="tiled", choices=["rowmajor", "tiled"],
                     help="layout of the resident output embedding (tiled: jet_tile_weights once, the default)")

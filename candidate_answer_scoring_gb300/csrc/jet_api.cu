@@ -73,16 +73,6 @@ bool head_use_dynamic(const Plan& p) {
   return p.pair && p.units > p.grid / 2;
 }
 
-int head_prefetch_kblocks(const Plan& p) {
-  static int env = -2;
-  if (env == -2) {
-    const char* v = std::getenv("JETSCORE_W_PREFETCH");
-    env = v ? std::atoi(v) : -1;
-  }
-  (void)p;
-  return env > 0 ? env : 0;
-}
-
 bool pdl_enabled() {
   static int on = -1;
   if (on < 0) on = std::getenv("JETSCORE_NO_PDL") ? 0 : 1;
@@ -263,7 +253,6 @@ int run_full_head(jet_ctx* c, const void* H, const void* W, int n_rows, float* l
   ha.zg = c->zg;
   ha.part = c->part;
   ha.err = c->err;
-  ha.pf_kblocks = head_prefetch_kblocks(ha.plan);
   ha.w_tiled = c->w_layout == JET_W_TILED ? 1 : 0;
   ha.sched = head_use_dynamic(plan) ? c->err + SCHED_WORD : nullptr;
   cudaError_t e;

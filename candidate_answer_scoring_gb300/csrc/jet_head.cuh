@@ -112,7 +112,6 @@ struct HeadArgs {
   float* zg;            // [n_tok] gathered logit of each scored token
   float2* part;         // per (unit, CTA of the pair, column half, row): (max, sum exp(z - max))
   int* err;
-  int pf_kblocks;       // L2 prefetch distance for W, in k-blocks of the CTA's stream (0: off)
   int w_tiled = 0;      // tmW is the 4-D map of a tiled W (jet_tile_weights)
   int* sched = nullptr; // paired head, several waves of units: counter (zeroed by the pre-pass)
                         // from which pairs take units after their first; NULL: static stride
@@ -124,12 +123,6 @@ bool head_use_dynamic(const Plan& p);
 
 // Host: whether the paired (2-SM) head serves N rows.
 bool head_use_pair(int N);
-
-// Host: L2 prefetch distance (k-blocks) for the head's W stream.  Off by
-// default: measured on GB300 it slowed the W-streaming head (two CTAs share
-// each W tile and both prefetch).  The environment variable
-// JETSCORE_W_PREFETCH sets a distance for experiments.
-int head_prefetch_kblocks(const Plan& p);
 
 // Decode unit u of the plan into (row tile, first vocab tile, end vocab tile).
 __host__ __device__ __forceinline__ void plan_unit(const Plan& p, int u, int& m, int& vt0, int& vt1) {

@@ -19,9 +19,11 @@
 // on the array.
 //
 // Set-up: in host code the array's name is only a host-side stand-in; its
-// device address is taken with cudaGetSymbolAddress, once per device, on the
-// first call made with that device current, and cached.  Make that first call
-// before any stream capture.
+// device address is taken with cudaGetSymbolAddress on the first call made in
+// each CUDA context on a device (with that device current) and cached, keyed
+// on the context's unique id, so a context created after cudaDeviceReset, or
+// a caller's own driver-API context, never receives an address from another
+// context.  Make that first call before any stream capture.
 #include <mutex>
 
 #include "jet_internal.cuh"
@@ -36,7 +38,11 @@ constexpr int NA_MAX_DEVICES = 64;
 
 constexpr size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 constexpr size_t OFF_ERR = 0;
-constexpr size_t OFF_ROW_PTR = align256(OFF_ERR + sizeof(int) * ERR_WORDS);
+// the error words and, after them, the head's unit counter err[SCHED_WORD]
+constexpr size_t ERR_BLOCK_BYTES = sizeof(int) * (SCHED_WORD + 1);
+constexpr size_t OFF_ROW_PTR = align256(OFF_ERR + ERR_BLOCK_BYTES);
+static_assert(OFF_ROW_PTR >= OFF_ERR + ERR_BLOCK_BYTES, "row offsets overlap the error block");
+static_assert(SCHED_WORD >= ERR_WORDS, "the unit counter follows the error words");
 constexpr size_t OFF_ROW_CUR = align256(OFF_ROW_PTR + sizeof(int) * (NA_MAX_POS + 1));
 constexpr size_t OFF_ROW_LIST = align256(OFF_ROW_CUR + sizeof(int) * (NA_MAX_POS + 1));
 constexpr size_t OFF_ZG = align256(OFF_ROW_LIST + sizeof(int2) * NA_MAX_POS);
@@ -49,29 +55,55 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-std::mutex g_mu;
-unsigned char* g_dev_addr[NA_MAX_DEVICES] = {};
-EncodeTiledFn g_encode = nullptr;
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
 
-// Device address of the scratch array on `dev` (which must be current).
+std::mutex g_mu;
+struct ScratchSlot {
+  unsigned long long ctx_id;   // unique id of the context the address belongs to
+  unsigned char* addr;         // device address of g_noalloc_scratch in that context (NULL: not looked up)
+};
+ScratchSlot g_slot[NA_MAX_DEVICES] = {};
+EncodeTiledFn g_encode = nullptr;
+CtxGetCurrentFn g_ctx_current = nullptr;
+CtxGetIdFn g_ctx_id = nullptr;
+
+template <typename Fn>
+bool driver_entry(const char* name, Fn* out) {
+  cudaDriverEntryPointQueryResult q;
+  void* fn = nullptr;
+  if (cudaGetDriverEntryPointByVersion(name, &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn)
+    return false;
+  *out = reinterpret_cast<Fn>(fn);
+  return true;
+}
+
+// Device address of the scratch array in the current context of `dev`
+// (which must be current).
 int scratch_address(int dev, unsigned char** out) {
   if (dev < 0 || dev >= NA_MAX_DEVICES) return JET_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_dev_addr[dev]) {
+  if (!g_encode && !driver_entry("cuTensorMapEncodeTiled", &g_encode)) return JET_ERR_CUDA;
+  if (!g_ctx_current && !driver_entry("cuCtxGetCurrent", &g_ctx_current)) return JET_ERR_CUDA;
+  if (!g_ctx_id && !driver_entry("cuCtxGetId", &g_ctx_id)) return JET_ERR_CUDA;
+  // The kernels run in the thread's current context.  When none is current
+  // yet, the runtime's first context-bound call (the symbol lookup) makes the
+  // device's primary context current, so look up first and read the id after.
+  CUcontext ctx = nullptr;
+  if (g_ctx_current(&ctx) != CUDA_SUCCESS) return JET_ERR_CUDA;
+  ScratchSlot& slot = g_slot[dev];
+  unsigned long long id = 0;
+  if (ctx && g_ctx_id(ctx, &id) != CUDA_SUCCESS) return JET_ERR_CUDA;
+  if (!ctx || !slot.addr || slot.ctx_id != id) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return JET_ERR_CUDA;
-    g_dev_addr[dev] = static_cast<unsigned char*>(p);
-  }
-  if (!g_encode) {
-    cudaDriverEntryPointQueryResult q;
-    void* fn = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
-            cudaSuccess ||
-        q != cudaDriverEntryPointSuccess || !fn)
+    if (!ctx && (g_ctx_current(&ctx) != CUDA_SUCCESS || !ctx || g_ctx_id(ctx, &id) != CUDA_SUCCESS))
       return JET_ERR_CUDA;
-    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    slot.addr = static_cast<unsigned char*>(p);
+    slot.ctx_id = id;
   }
-  *out = g_dev_addr[dev];
+  *out = slot.addr;
   return JET_OK;
 }
 
@@ -145,7 +177,6 @@ extern "C" int jet_score_tokens_noalloc(const void* H, const void* W, int d, int
   ha.zg = zg;
   ha.part = part;
   ha.err = err;
-  ha.pf_kblocks = head_prefetch_kblocks(ha.plan);
   ha.sched = head_use_dynamic(plan) ? err + SCHED_WORD : nullptr;
   if (launch_head(tmH, tmW, ha, st) != cudaSuccess) {
     cudaStreamSynchronize(st);

@@ -104,14 +104,6 @@ __device__ __forceinline__ void tma_load_4d_pair(void* dst, const CUtensorMap* m
       : "memory");
 }
 
-// Bring a tile into L2 ahead of its TMA load (no shared-memory destination).
-__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x, int y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(x), "r"(y)
-               : "memory");
-}
-
 // ---- cluster ------------------------------------------------------------------
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
@@ -478,11 +470,6 @@ __global__ void __launch_bounds__(HEAD_THREADS, 1)
                 if (a.w_tiled) tma_load_4d(dB + j * SH::B_KB_BYTES, &tmW, kb + j, b_row >> 7, &full[stage], pol_w);
                 else tma_load_2d(dB + j * SH::B_KB_BYTES, &tmW, (kb + j) * BK, b_row, &full[stage], pol_w);
               }
-            }
-            if (a.pf_kblocks > 0 && !a.w_tiled) {   // optional: more W bytes in flight than the ring holds
-              const int ip = (vt - vt0) * kblocks + kb + a.pf_kblocks;
-              const int vtp = vt0 + ip / kblocks;
-              if (vtp < vt1) tma_prefetch_l2_2d(&tmW, (ip % kblocks) * BK, vtp * BN + (int)rank * SH::B_ROWS);
             }
             issued_mask |= 1u << stage;
             issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);

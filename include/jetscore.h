@@ -38,6 +38,17 @@
  *     for the stream once at the end and return that word.  On any error the
  *     outputs are unspecified.  Nothing in the library traps or asserts on the
  *     device; every device-side wait is bounded and reports JET_ERR_TIMEOUT.
+ *
+ * Diagnostic environment variables (read once per process; NOT part of the
+ * ABI, for measuring and testing the library's own variants; results are
+ * identical under every setting):
+ *   JETSCORE_NO_PDL=1     launch every kernel with plain stream ordering
+ *                         instead of programmatic dependent launch;
+ *   JETSCORE_HEAD_PAIR=0|1 force the one-CTA (0) or the paired 2-SM (1)
+ *                         full-vocabulary head for every batch size;
+ *   JETSCORE_HEAD_DYN=0   paired head with several waves of units: take
+ *                         units in a fixed stride order instead of from the
+ *                         device counter.
  */
 #ifndef JETSCORE_H
 #define JETSCORE_H
@@ -348,9 +359,11 @@ int jet_selftest_wait_timeout(jet_ctx *ctx, int limit_us, void *cuda_stream);
  * the process exits; it bounds a call to n_pos <= JET_NOALLOC_MAX_POS
  * (larger batches return JET_ERR_WORKSPACE).  All calls share that array:
  * calls whose GPU work overlaps (other streams or host threads) race on it.
- * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) and caches it; make that first call before any
- * stream capture.  Synchronous; returns JET_OK or a status as above.
+ * The first call in each CUDA context on a device looks up the array's
+ * device address (cudaGetSymbolAddress) and caches it for that context (a
+ * context made after cudaDeviceReset looks it up again); make that first call
+ * before any stream capture.  Synchronous; returns JET_OK or a status as
+ * above.
  */
 #define JET_NOALLOC_MAX_POS 4096
 #define JET_NOALLOC_MAX_UNITS 1024

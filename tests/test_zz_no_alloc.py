@@ -90,3 +90,35 @@ def test_noalloc_many_waves_matches_fp32_torch():
     ref_lp = z.gather(1, tok.long()[:, None])[:, 0] - ref_lse
     assert (lse - ref_lse).abs().max().item() <= TOL
     assert (logp - ref_lp).abs().max().item() <= TOL
+
+
+def test_noalloc_call_after_a_rejected_call():
+    """A call the device pre-pass rejects (a token id equal to V) leaves its
+    error word and, for a plan with several waves of units, the unit counter
+    in the shared static array; the next valid call over several waves must
+    start clean and match jet_score_tokens."""
+    jet, fn = _noalloc_fn()
+    dev = torch.device("cuda", 0)
+    stream = C.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+    d, V, n = 128, 30000, 4096
+    rng = np.random.default_rng(12)
+    W = torch.from_numpy(wk.gen_W(612, V, d).view(np.int16)).to(dev).view(torch.bfloat16)
+    H = torch.from_numpy(wk.to_bf16_bits(rng.normal(size=(n, d)).astype(np.float32)).view(np.int16))
+    H = H.to(dev).view(torch.bfloat16)
+    tok = torch.from_numpy(rng.integers(0, V, size=n).astype(np.int32)).to(dev)
+    bad = tok.clone()
+    bad[n // 2] = V
+    logp = torch.full((n,), float("nan"), device=dev)
+    lse = torch.full((n,), float("nan"), device=dev)
+    args = lambda t: (C.c_void_p(H.data_ptr()), C.c_void_p(W.data_ptr()), d, V, C.c_void_p(t.data_ptr()), n,
+                      C.c_void_p(logp.data_ptr()), C.c_void_p(lse.data_ptr()), stream)
+    rc = fn(*args(bad))
+    assert rc == -2, f"expected JET_ERR_TOKEN_RANGE, got {rc} ({jet.status_string(rc)})"
+    sc = jet.JetScorer(d, V, n, n)
+    info = sc.plan_info(n)
+    assert info["units"] > info["ctas"] // 2, info      # the counter path
+    rc = fn(*args(tok))
+    assert rc == 0, f"status {rc} ({jet.status_string(rc)}) after a rejected call"
+    ref_lp, ref_lse = sc.score_tokens(H, W, tok, want_lse=True)
+    assert (logp - ref_lp).abs().max().item() <= TOL
+    assert (lse - ref_lse).abs().max().item() <= TOL
