@@ -639,6 +639,47 @@ def op_arm(args):
                     config={"workload": "wide schema: %d sets, %d candidates; gold drawn from q at T0 = %.3f"
                                         % (wl.n_sets, wl.n_cand, T0)},
                     roofline={"bound": "latency", "note": "one CTA, bracketed Newton on 1/T; synchronous call"})
+    elif args.op == "restricted":
+        # restricted mode on the binary batch's shape (256 questions, one row
+        # each, d=2560, V=248320) over unions of several sizes: each question a
+        # binary pair of codes drawn from the union
+        line.update(metric="restricted-mode candidate tokens scored per second", unit="tokens/s", per_union={})
+        W_dev = None
+        for n_union in [int(x) for x in args.unions.split(",")]:
+            wl = wk.union_choice(256, n_union)
+            if W_dev is None:
+                W_dev = t(wl.W.view(np.int16)).view(torch.bfloat16)
+            sc = jet.JetScorer(wl.d, wl.V, wl.N, wl.n_tok)
+            Wt = sc.tile_weights(W_dev) if args.w_layout == "tiled" else W_dev
+            x = [t(a) for a in (wl.tok_row, wl.tok_ids, wl.cand_offsets, wl.set_offsets, wl.kind, wl.union_ids)]
+            H = t(wl.H.view(np.int16)).view(torch.bfloat16)
+            o = sc.alloc_outputs(wl.N, wl.n_tok, wl.n_cand, wl.n_sets)
+            fn = lambda: sc.score_sets(H, Wt, x[0], x[1], x[2], x[3], x[4], wl.T, wl.mode, x[5], out=o, sync=False)
+            ms = time_op(fn, K, W)
+            sc.profile(True)
+            time_op(fn, K, 0)
+            prof = sc.profile_read()
+            sc.profile(False)
+            rc = sc.sync_status()
+            if rc != 0:
+                raise RuntimeError(f"restricted |U|={n_union}: status {rc}")
+            kern = {k: v["ms"] * 1e3 / K for k, v in prof.items() if isinstance(v, dict) and v["launches"]}
+            path = "tcgen05 head over the staged union" if prof["head"]["launches"] else "mma.sync union kernel"
+            proj_us = kern.get("head", kern.get("restricted", 0.0))
+            nbytes = 2.0 * n_union * wl.d + 2.0 * wl.N * wl.d
+            flops = 2.0 * wl.N * wl.d * n_union
+            line["per_union"][str(n_union)] = {
+                "path": path, "us_per_call": ms * 1e3, "tokens_per_s": wl.n_tok / (ms / 1e3),
+                "kernel_us": kern, "projection_us": proj_us,
+                "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
+                "projection_gbs": nbytes / (proj_us / 1e6) / 1e9 if proj_us else None,
+                "projection_tflops": flops / (proj_us / 1e6) / 1e12 if proj_us else None,
+                "roofline_us": max(nbytes / (peaks["hbm"] * 1e9), flops / (peaks["bf16"] * 1e12)) * 1e6}
+            sc.close()
+            del Wt
+        line["config"] = {"workload": "256 questions x binary pair of codes from the union, d=2560, V=248320, "
+                                      "one row per question, T=2.179; asynchronous calls back to back",
+                          "weights_layout": args.w_layout, "peaks": peaks["source"]}
     elif args.op == "layer_sensitivity":
         rng = np.random.default_rng(0)
         n, L, m = 4096, 64, 64
@@ -676,8 +717,10 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--dedup", action="store_true",
                     help="score each distinct hidden row once (jet_dedup_rows before every step)")
-    ap.add_argument("--op", default=None, choices=["dedup", "fit_temperature", "layer_sensitivity"],
-                    help="time one of the widened ops instead of the scoring path")
+    ap.add_argument("--op", default=None, choices=["dedup", "fit_temperature", "layer_sensitivity", "restricted"],
+                    help="time one of the widened ops, or restricted mode over larger unions, instead of the "
+                         "scoring path")
+    ap.add_argument("--unions", default="26,256,600,4096", help="union sizes for --op restricted")
     return ap.parse_args(argv)
 
 

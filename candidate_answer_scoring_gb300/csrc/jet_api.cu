@@ -73,6 +73,22 @@ bool head_use_dynamic(const Plan& p) {
   return p.pair && p.units > p.grid / 2;
 }
 
+// Restricted mode on the tensor-core head (the union gathered into a staging
+// copy and used as the vocabulary) for unions of at least this many codes;
+// smaller unions take the two-launch mma.sync path.  JETSCORE_RESTRICTED_TC=0/1
+// forces a path (diagnostics; 1 applies wherever the staging copy fits).
+constexpr int RESTRICTED_TC_MIN_UNION = 256;
+
+bool restricted_use_tc(int n_union, int staging_rows) {
+  static int env = -2;
+  if (env == -2) {
+    const char* v = std::getenv("JETSCORE_RESTRICTED_TC");
+    env = v ? std::atoi(v) : -1;
+  }
+  if (n_union > staging_rows || env == 0) return false;
+  return env > 0 || n_union >= RESTRICTED_TC_MIN_UNION;
+}
+
 bool pdl_enabled() {
   static int on = -1;
   if (on < 0) on = std::getenv("JETSCORE_NO_PDL") ? 0 : 1;
@@ -126,6 +142,10 @@ struct jet_ctx {
   // [max_rows, d] staging copy of H: host inputs (jet_score_sets_host) and
   // gathered rows (jet_score_sets_gather)
   uint16_t* stH = nullptr;
+  // [wU_rows, d] staging copy of the union's rows of W (restricted mode on the
+  // tensor-core head); wU_rows = min(V, JET_MAX_UNION)
+  uint16_t* wU = nullptr;
+  int wU_rows = 0;
   // jet_score_sets_host packs the small inputs into one pinned block (one
   // copy in) and lays the requested outputs out behind the error word in one
   // device block (one copy out, status included)
@@ -140,7 +160,7 @@ struct jet_ctx {
   // temperature fitting
   double *fit_res = nullptr, *h_fit = nullptr;   // device [3], pinned host [3]
   // schedule cache
-  int plan_rows = -1;
+  int plan_rows = -1, plan_V = -1;
   Plan plan;
   // kernel timing (jet_profile_enable)
   bool prof = false;
@@ -223,29 +243,31 @@ int encode_kmajor(jet_ctx* c, CUtensorMap* map, const void* base, int rows, int 
   return r == CUDA_SUCCESS ? JET_OK : JET_ERR_CUDA;
 }
 
-const Plan& plan_for(jet_ctx* c, int n_rows) {
-  if (c->plan_rows != n_rows) {
-    c->plan = make_plan(n_rows, c->V, c->d, c->num_sms, c->units_cap, head_use_pair(n_rows));
+const Plan& plan_for(jet_ctx* c, int n_rows, int V) {
+  if (c->plan_rows != n_rows || c->plan_V != V) {
+    c->plan = make_plan(n_rows, V, c->d, c->num_sms, c->units_cap, head_use_pair(n_rows));
     c->plan_rows = n_rows;
+    c->plan_V = V;
   }
   return c->plan;
 }
 
-// Full-vocabulary head and merge for the rows/tokens the pre-pass listed.
-// lse_row NULL: one token per row, logp[r] written by the merge; else the
-// merge leaves each row's lse in lse_row for the set kernel.
-int run_full_head(jet_ctx* c, const void* H, const void* W, int n_rows, float* logp, float* lse,
-                  float* lse_row, cudaStream_t st) {
-  const Plan& plan = plan_for(c, n_rows);
+// Tensor-core head and merge for the rows/tokens the pre-pass listed, over
+// the V rows of W (the full vocabulary in the caller's layout, or the staged
+// union, row-major).  lse_row NULL: one token per row, logp[r] written by the
+// merge; else the merge leaves each row's lse in lse_row for the set kernel.
+int run_full_head(jet_ctx* c, const void* H, const void* W, int V, bool w_tiled, int n_rows, float* logp,
+                  float* lse, float* lse_row, cudaStream_t st) {
+  const Plan& plan = plan_for(c, n_rows, V);
   CUtensorMap tmH, tmW;
   int rc = encode_kmajor(c, &tmH, H, n_rows, BM);
   if (rc != JET_OK) return rc;
   const int w_box = plan.pair ? HeadShape<true>::B_ROWS : HeadShape<false>::B_ROWS;
-  rc = c->w_layout == JET_W_TILED ? encode_tiled_w(c, &tmW, W, w_box) : encode_kmajor(c, &tmW, W, c->V, w_box);
+  rc = w_tiled ? encode_tiled_w(c, &tmW, W, w_box) : encode_kmajor(c, &tmW, W, V, w_box);
   if (rc != JET_OK) return rc;
   HeadArgs ha;
   ha.N = n_rows;
-  ha.V = c->V;
+  ha.V = V;
   ha.d = c->d;
   ha.plan = plan;
   ha.row_ptr = c->row_ptr;
@@ -253,7 +275,7 @@ int run_full_head(jet_ctx* c, const void* H, const void* W, int n_rows, float* l
   ha.zg = c->zg;
   ha.part = c->part;
   ha.err = c->err;
-  ha.w_tiled = c->w_layout == JET_W_TILED ? 1 : 0;
+  ha.w_tiled = w_tiled ? 1 : 0;
   ha.sched = head_use_dynamic(plan) ? c->err + SCHED_WORD : nullptr;
   cudaError_t e;
   {
@@ -321,7 +343,10 @@ int score_sets_enqueue(jet_ctx* c, const void* H, const void* W, int n_rows, con
   sa.tok_row = nullptr;
   sa.err = c->err;
 
-  if (mode == JET_MODE_RESTRICTED) {
+  // restricted mode over a large union: the union's rows of W are staged and
+  // the tensor-core head runs with the union as its vocabulary
+  const bool union_tc = mode == JET_MODE_RESTRICTED && restricted_use_tc(n_union, c->wU_rows);
+  if (mode == JET_MODE_RESTRICTED && !union_tc) {
     // restricted head (zeroes the error word), then validation + set rules
     RestrictedSetArgs rs;
     RestrictedArgs& ra = rs.r;
@@ -361,6 +386,12 @@ int score_sets_enqueue(jet_ctx* c, const void* H, const void* W, int n_rows, con
         cudaSuccess)
       return JET_ERR_CUDA;
   }
+  if (union_tc) {
+    ProfScope ps(c, K_PREP, st);
+    if (launch_union_rows(static_cast<const uint16_t*>(W), c->V, c->d, c->w_layout == JET_W_TILED ? 1 : 0,
+                          union_ids, n_union, c->wU, c->umap, st) != cudaSuccess)
+      return JET_ERR_CUDA;
+  }
   PrepArgs pa;
   pa.n_rows = n_rows;
   pa.n_tok = n_tok;
@@ -378,12 +409,19 @@ int score_sets_enqueue(jet_ctx* c, const void* H, const void* W, int n_rows, con
   pa.row_cur = c->row_cur;
   pa.row_list = c->row_list;
   pa.err = c->err;
+  if (union_tc) {
+    pa.union_ids = union_ids;
+    pa.n_union = n_union;
+    pa.umap = c->umap;
+  }
   {
     ProfScope ps(c, K_PREP, st);
     if (launch_prep(pa, st) != cudaSuccess) return JET_ERR_CUDA;
   }
-  const int rc = run_full_head(c, row_index ? static_cast<const void*>(c->stH) : H, W, n_rows, sa.logp, o.lse,
-                               c->lse_row, st);
+  const void* Hs = row_index ? static_cast<const void*>(c->stH) : H;
+  const int rc = union_tc ? run_full_head(c, Hs, c->wU, n_union, false, n_rows, sa.logp, o.lse, c->lse_row, st)
+                          : run_full_head(c, Hs, W, c->V, c->w_layout == JET_W_TILED, n_rows, sa.logp, o.lse,
+                                          c->lse_row, st);
   if (rc != JET_OK) return rc;
   sa.zg = c->zg;            // logp = z - lse(row), formed by the set kernel
   sa.lse_row = c->lse_row;
@@ -477,6 +515,8 @@ int jet_create(jet_ctx** out, int d, int V, int max_rows, int max_tokens, int de
   A(dalloc(&c->conf, Tk));
   A(dalloc(&c->mass, Tk));
   A(dalloc(&c->stH, R * (size_t)d));
+  c->wU_rows = std::min(V, JET_MAX_UNION);
+  A(dalloc(&c->wU, (size_t)c->wU_rows * d));
   A(dalloc(&c->d_in, c->in_cap));
   A(cudaMallocHost(reinterpret_cast<void**>(&c->h_in), c->in_cap));
   A(cudaMallocHost(reinterpret_cast<void**>(&c->h_out), c->out_cap));
@@ -505,7 +545,7 @@ void jet_destroy(jet_ctx* c) {
   DeviceGuard g(c->device);
   cudaDeviceSynchronize();
   void* ptrs[] = {c->io_dev, c->row_ptr, c->row_cur, c->row_list, c->iscratch, c->lse_row, c->umap, c->zu, c->zg, c->part, c->hash,
-                  c->lse, c->logp, c->s, c->q, c->qe, c->dec, c->expd, c->conf, c->mass, c->stH,
+                  c->lse, c->logp, c->s, c->q, c->qe, c->dec, c->expd, c->conf, c->mass, c->stH, c->wU,
                   c->d_in,
                   c->dd_hash, c->dd_keys, c->dd_vals, c->dd_rep, c->dd_rank, c->dd_tiles};
   for (void* p : ptrs)
@@ -674,7 +714,7 @@ int jet_selftest_wait_timeout(jet_ctx* c, int limit_us, void* stream) {
 
 int jet_plan_info(jet_ctx* c, int n_rows, int* info) {
   if (!c || !info || n_rows < 1 || n_rows > c->max_rows) return JET_ERR_ARG;
-  const Plan& p = plan_for(c, n_rows);
+  const Plan& p = plan_for(c, n_rows, c->V);
   const int v[8] = {p.n_mt, p.n_vt, p.S, p.Gm, p.units, p.grid, plan_tile_rows(p), BN};
   std::memcpy(info, v, sizeof v);
   return JET_OK;
@@ -796,7 +836,7 @@ int jet_score_tokens(jet_ctx* c, const void* H, const void* W, const int32_t* to
     ProfScope ps(c, K_PREP, st);
     if (launch_prep(pa, st) != cudaSuccess) return JET_ERR_CUDA;
   }
-  int rc = run_full_head(c, H, W, n_pos, logp, lse, nullptr, st);
+  int rc = run_full_head(c, H, W, c->V, c->w_layout == JET_W_TILED, n_pos, logp, lse, nullptr, st);
   if (rc != JET_OK) {
     cudaStreamSynchronize(st);
     return rc;

@@ -19,8 +19,21 @@ struct PrepArgs {
   int* row_cur;    // [n_rows+1] scratch counters
   int2* row_list;  // [n_tok]
   int* err;
+  // restricted mode on the tensor-core head (launch_union_rows ran first):
+  // the union is the vocabulary.  Adds the restricted checks (union ids in
+  // range and distinct, one token per candidate, every token in the union)
+  // and lists each token under its union position instead of its id.
+  const int32_t* union_ids = nullptr;   // NULL: full vocabulary
+  int n_union = 0;
+  const int* umap = nullptr;            // [V] token id -> union position (launch_union_rows)
 };
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t st);
+
+// Restricted mode on the tensor-core head: wU[u] = W[union_ids[u]] (row-major
+// [n_union, d]; W row-major or tiled), and umap[union_ids[u]] = u.  Ids
+// outside [0, V) give a zero row and no map entry (the pre-pass reports them).
+cudaError_t launch_union_rows(const uint16_t* W, int V, int d, int w_tiled, const int32_t* union_ids, int n_union,
+                              uint16_t* wU, int* umap, cudaStream_t st);
 
 // Tiled copy of W (layout stated in jetscore.h, "Tiled weights").
 cudaError_t launch_tile_weights(const uint16_t* W, int V, int d, uint16_t* W_tiled, cudaStream_t st);

@@ -23,6 +23,12 @@ __device__ __forceinline__ int row_of(const PrepArgs& a, int j) {
   return a.tok_row ? a.tok_row[j] : j;
 }
 
+// The column token j is gathered from: its id, or in restricted mode its
+// union position (read only after validation has passed).
+__device__ __forceinline__ int list_key(const PrepArgs& a, int j) {
+  return a.union_ids ? a.umap[a.tok_ids[j]] : a.tok_ids[j];
+}
+
 // Dynamic shared memory: [n_rows + 1] per-row counters when SMEM_COUNTS.
 // Kept small so that the head kernel's CTA can share an SM with this one.
 template <bool SMEM_COUNTS>
@@ -47,10 +53,25 @@ __global__ void __launch_bounds__(PREP_THREADS) prep_kernel(PrepArgs a) {
   __syncthreads();
 
   // scored tokens: id in [0, V), row in [0, n_rows); is tok_row non-decreasing?
+  // Restricted mode: the id's union position (a map entry is trusted only
+  // where union_ids agrees, so entries left by earlier calls are harmless).
   for (int j = tid; j < a.n_tok; j += nth) {
     const int t = a.tok_ids[j], r = row_of(a, j);
-    if (t < 0 || t >= a.V || r < 0 || r >= a.n_rows) set_error(err, JET_ERR_TOKEN_RANGE, j);
+    if (t < 0 || t >= a.V || r < 0 || r >= a.n_rows) {
+      set_error(err, JET_ERR_TOKEN_RANGE, j);
+    } else if (a.union_ids) {
+      const int pos = a.umap[t];
+      if (pos < 0 || pos >= a.n_union || a.union_ids[pos] != t) set_error(err, JET_ERR_NOT_IN_UNION, j);
+    }
     if (!identity && j > 0 && a.tok_row[j - 1] > r) s_unsorted = 1;
+  }
+
+  // restricted mode: union ids in [0, V) and distinct (a repeated id keeps
+  // one map position, so another of its positions does not map back)
+  for (int u = tid; u < (a.union_ids ? a.n_union : 0); u += nth) {
+    const int t = a.union_ids[u];
+    if (t < 0 || t >= a.V) set_error(err, JET_ERR_TOKEN_RANGE, u);
+    else if (a.umap[t] != u) set_error(err, JET_ERR_NOT_IN_UNION, u);
   }
 
   // gathered rows: every index within the source array
@@ -67,8 +88,9 @@ __global__ void __launch_bounds__(PREP_THREADS) prep_kernel(PrepArgs a) {
       if (a.set_offsets[0] != 0 || a.set_offsets[a.n_sets] != a.n_cand) set_error(err, JET_ERR_OFFSETS, 0);
     }
     for (int c = tid; c < a.n_cand; c += nth) {
-      const int len = a.cand_offsets[c + 1] - a.cand_offsets[c];
-      if (len < 1) set_error(err, JET_ERR_OFFSETS, c);
+      const int t0 = a.cand_offsets[c], t1 = a.cand_offsets[c + 1];
+      if (!(t0 >= 0 && t0 < t1 && t1 <= a.n_tok)) set_error(err, JET_ERR_OFFSETS, c);
+      else if (a.union_ids && t1 - t0 != 1) set_error(err, JET_ERR_MODE, c);   // restricted: one token each
     }
     for (int k = tid; k < a.n_sets; k += nth) {
       const int K = a.set_offsets[k + 1] - a.set_offsets[k];
@@ -86,7 +108,7 @@ __global__ void __launch_bounds__(PREP_THREADS) prep_kernel(PrepArgs a) {
   if (identity) {                                    // one token per row, in row order
     for (int i = tid; i < a.n_tok; i += nth) {
       a.row_ptr[i] = i;
-      a.row_list[i] = make_int2(a.tok_ids[i], i);
+      a.row_list[i] = make_int2(list_key(a, i), i);
     }
     if (tid == 0) a.row_ptr[a.n_rows] = a.n_tok;
     return;
@@ -100,7 +122,7 @@ __global__ void __launch_bounds__(PREP_THREADS) prep_kernel(PrepArgs a) {
       for (int rr = rp + 1; rr <= r; ++rr) a.row_ptr[rr] = j;       // rows rp+1 .. r start at j
       if (j == a.n_tok - 1)
         for (int rr = r + 1; rr <= a.n_rows; ++rr) a.row_ptr[rr] = a.n_tok;
-      a.row_list[j] = make_int2(a.tok_ids[j], j);
+      a.row_list[j] = make_int2(list_key(a, j), j);
     }
     __syncthreads();
     for (int r = tid; r < a.n_rows; r += nth) {      // order each row's tokens by id
@@ -160,7 +182,7 @@ __global__ void __launch_bounds__(PREP_THREADS) prep_kernel(PrepArgs a) {
   // scatter (token id, token index) into each row's slot range
   for (int j = tid; j < a.n_tok; j += nth) {
     const int pos = atomicAdd(&cnt[row_of(a, j)], 1);
-    a.row_list[pos] = make_int2(a.tok_ids[j], j);
+    a.row_list[pos] = make_int2(list_key(a, j), j);
   }
   __syncthreads();
 

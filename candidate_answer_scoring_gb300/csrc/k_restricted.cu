@@ -468,7 +468,39 @@ __global__ void __launch_bounds__(32 * RS_WARPS) restricted_sets_kernel(const Re
   set_rules_warp(sa, k, lane, c0, c1);
 }
 
+// Larger unions run on the full-vocabulary tensor-core head with the union as
+// its vocabulary: this kernel stages the union's rows of W contiguously (the
+// head's TMA loads read a row-major [n_union, d] operand) and records each
+// id's position for the pre-pass.  One warp per union row, 16-byte copies.
+__global__ void __launch_bounds__(256) union_rows_kernel(const uint4* W, int V, int d, int w_tiled,
+                                                         const int32_t* union_ids, int n_union, uint4* wU,
+                                                         int* umap) {
+  pdl_wait();      // earlier work on the stream (readers of wU and umap) is complete
+  pdl_trigger();   // the pre-pass may start; it waits for this grid before anything reads wU
+  const int lane = threadIdx.x & 31, nvec = d / 8;
+  const bool tiled = w_tiled != 0;
+  for (int u = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; u < n_union; u += (gridDim.x * blockDim.x) >> 5) {
+    const int t = union_ids[u];
+    uint4* o = wU + (size_t)u * nvec;
+    if (t < 0 || t >= V) {   // reported by the pre-pass; the row is never used
+      for (int k = lane; k < nvec; k += 32) o[k] = make_uint4(0, 0, 0, 0);
+      continue;
+    }
+    if (lane == 0) umap[t] = u;
+    const size_t wb = w_row_base(t, d, tiled);
+    for (int k = lane; k < nvec; k += 32) o[k] = W[w_vec(wb, k, tiled)];
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_union_rows(const uint16_t* W, int V, int d, int w_tiled, const int32_t* union_ids, int n_union,
+                              uint16_t* wU, int* umap, cudaStream_t st) {
+  if (n_union <= 0) return cudaSuccess;
+  const int blocks = (n_union + 7) / 8 < 1184 ? (n_union + 7) / 8 : 1184;   // 8 rows per block
+  return launch_dependent(union_rows_kernel, dim3(blocks), dim3(256), 0, st, reinterpret_cast<const uint4*>(W), V,
+                          d, w_tiled, union_ids, n_union, reinterpret_cast<uint4*>(wU), umap);
+}
 
 cudaError_t launch_restricted(const RestrictedArgs& a, cudaStream_t st) {
   if (a.N <= 0) return cudaSuccess;

@@ -40,15 +40,18 @@
  *     device; every device-side wait is bounded and reports JET_ERR_TIMEOUT.
  *
  * Diagnostic environment variables (read once per process; NOT part of the
- * ABI, for measuring and testing the library's own variants; results are
- * identical under every setting):
+ * ABI, for measuring and testing the library's own variants; every setting
+ * gives results within the library's stated tolerances):
  *   JETSCORE_NO_PDL=1     launch every kernel with plain stream ordering
  *                         instead of programmatic dependent launch;
  *   JETSCORE_HEAD_PAIR=0|1 force the one-CTA (0) or the paired 2-SM (1)
  *                         full-vocabulary head for every batch size;
  *   JETSCORE_HEAD_DYN=0   paired head with several waves of units: take
  *                         units in a fixed stride order instead of from the
- *                         device counter.
+ *                         device counter;
+ *   JETSCORE_RESTRICTED_TC=0|1 restricted mode: the mma.sync union kernel
+ *                         (0) or the tcgen05 head over the staged union (1)
+ *                         for every union size (default: by union size).
  */
 #ifndef JETSCORE_H
 #define JETSCORE_H
@@ -88,7 +91,8 @@ enum { JET_MODE_FULL = 0, JET_MODE_RESTRICTED = 1 };
  * shape [V, d], and allocate its device workspace for up to `max_rows` hidden
  * rows and `max_tokens` scored tokens per call (candidates and sets are bounded
  * by max_tokens as every candidate has >= 1 token).  Also allocates device
- * staging buffers of that size for jet_score_sets_host.
+ * staging buffers of that size for jet_score_sets_host, and one of
+ * min(V, JET_MAX_UNION) rows of W for restricted mode over large unions.
  * Errors: JET_ERR_ARG (sizes), JET_ERR_UNSUPPORTED (not sm_103), JET_ERR_CUDA.
  * On success *out owns the workspace until jet_destroy.
  */
@@ -168,7 +172,11 @@ typedef struct {
  *       JET_MODE_RESTRICTED: normalise over union_ids[n_union] (distinct ids,
  *       1 <= n_union <= JET_MAX_UNION); every candidate is one token of the
  *       union (PARALLEL_SCORING page, "Execution" step 5).  union_ids is ignored
- *       in full mode.
+ *       in full mode.  Unions of fewer than 256 codes are projected by a small
+ *       tensor-core kernel (mma.sync); larger ones are copied into the
+ *       context's staging rows and projected by the full-vocabulary tcgen05
+ *       head with the union as its vocabulary (JETSCORE_RESTRICTED_TC=0|1
+ *       forces either, for diagnostics).
  * out -- host struct of device pointers; any member may be NULL.
  * Empty batches (n_tok == 0 with n_cand == n_sets == 0) return JET_OK.
  * Synchronous: waits for `cuda_stream` once, then returns the device status.
@@ -188,7 +196,8 @@ int jet_score_sets(jet_ctx *ctx, const void *H_bf16, const void *W_bf16, int n_r
  * scores use each row's last valid position).  Row i of the problem is
  * H_src[row_index[i]].  Full mode copies the gathered rows once into the
  * context's staging buffer (one warp per row) and streams them from there
- * with tiled loads; restricted mode reads them in place.
+ * with tiled loads, as does restricted mode over unions on the tcgen05 head;
+ * restricted mode over smaller unions reads them in place.
  *   H_src_bf16 [n_src_rows, d] bf16 (device, 16-byte aligned);
  *   row_index [n_rows] int32 (device), each in
  *   [0, n_src_rows); rows may repeat.  Every other argument is as in

@@ -1,0 +1,215 @@
+"""Restricted mode over larger unions: from 256 codes the union's rows of W are
+staged and the tcgen05 head runs with the union as its vocabulary (PARALLEL_
+SCORING page, "Execution" steps 5-6: project the final hidden states onto the
+gathered union, softmax over each field's candidates).  Parity with the oracle
+element by element, both projection paths forced on the sizes the other one
+serves, the layouts that reach the staging copy (tiled W, gathered rows), and
+the restricted-mode status codes on this path."""
+import os
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wk
+from parity import check_duplicates, compare
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+OK, ARG, TOKEN, OFFSETS, MODE, UNION = 0, -1, -2, -3, -4, -5
+
+
+@pytest.fixture(scope="module")
+def jet():
+    import candidate_answer_scoring_gb300 as jet
+    jet.load()
+    return jet
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def args_of(wl, **over):
+    a = dict(H=dev(wl.H.view(np.int16)).view(torch.bfloat16), W=dev(wl.W.view(np.int16)).view(torch.bfloat16),
+             tok_row=dev(wl.tok_row), tok_ids=dev(wl.tok_ids), cand_offsets=dev(wl.cand_offsets),
+             set_offsets=dev(wl.set_offsets), kind=dev(wl.kind), T=wl.T, mode=wl.mode,
+             union_ids=None if wl.union_ids is None else dev(wl.union_ids))
+    a.update(over)
+    return a
+
+
+def run(sc, a):
+    out = sc.score_sets(a["H"], a["W"], a["tok_row"], a["tok_ids"], a["cand_offsets"], a["set_offsets"], a["kind"],
+                        a["T"], a["mode"], a["union_ids"])
+    torch.cuda.synchronize()
+    return {k: v.cpu().numpy() for k, v in out.items()}
+
+
+def status(jet, sc, a):
+    try:
+        run(sc, a)
+        return OK
+    except jet.JetError as e:
+        return e.status
+
+
+def uses_union_head(jet, sc, a):
+    """Whether the call ran the tcgen05 head (the library's launch record)."""
+    sc.profile(True)
+    run(sc, a)
+    prof = sc.profile_read()
+    sc.profile(False)
+    return prof["head"]["launches"] > 0
+
+
+@pytest.mark.parametrize("n_union,K,d,V,n_q", [
+    (256, (2, 2), 128, 3000, 300),      # the smallest union on the tensor-core head; 2 row tiles
+    (600, (2, 9), 512, 20000, 120),     # a ragged union tile (600 = 2 x 256 + 88)
+    (4096, (2, 6), 256, 9000, 500),     # the largest accepted union
+])
+def test_union_head_matches_oracle(jet, n_union, K, d, V, n_q):
+    wl = wk.union_choice(n_q, n_union, K=K, d=d, V=V, T=1.7, seed_offset=n_union)
+    sc = jet.JetScorer(d, V, wl.N, wl.n_tok)
+    a = args_of(wl)
+    assert uses_union_head(jet, sc, a)
+    gpu = run(sc, a)
+    compare(wl, gpu, oracle.score_workload(wl))
+
+
+def test_union_head_duplicates_tie_and_repeat_bitwise(jet):
+    """Sets holding the same code twice tie bit for bit (one row, one column),
+    and a repeated call gives the same bits."""
+    wl = wk.union_choice(200, 300, K=(3, 6), d=128, V=4000, seed_offset=9)
+    co, so = wl.cand_offsets, wl.set_offsets
+    ids = wl.tok_ids.copy()
+    for k in range(0, wl.n_sets, 3):                   # every third set: its last code repeats its first
+        ids[co[so[k + 1] - 1]] = ids[co[so[k]]]
+    wl = wk.Workload(wl.name + "-dup", wl.d, wl.V, wl.H, wl.W, wl.tok_row, ids, co, so, wl.kind, wl.T, wl.mode,
+                     wl.union_ids, dict(wl.info))
+    sc = jet.JetScorer(wl.d, wl.V, wl.N, wl.n_tok)
+    a = args_of(wl)
+    gpu = run(sc, a)
+    compare(wl, gpu, oracle.score_workload(wl))
+    assert check_duplicates(wl, gpu) >= 1
+    again = run(sc, a)
+    for k in gpu:
+        np.testing.assert_array_equal(again[k], gpu[k])
+
+
+def test_union_head_equals_full_mode_when_union_is_vocab(jet):
+    """U = the whole vocabulary in id order: the staged copy equals W, so the
+    head runs the same schedule over the same operands and the results are
+    bit-identical to full mode."""
+    base = wk.binary_batch(n_questions=300, random_pairs=True, d=128, V=3000)
+    sc = jet.JetScorer(base.d, base.V, base.N, base.n_tok)
+    full = run(sc, args_of(base))
+    rest = base.with_mode(wk.MODE_RESTRICTED, base.T, np.arange(base.V, dtype=np.int32))
+    a = args_of(rest)
+    assert uses_union_head(jet, sc, a)
+    got = run(sc, a)
+    for k in ("logp", "lse", "s", "q", "q_equiv", "decision", "expected", "confidence", "mass"):
+        np.testing.assert_array_equal(got[k], full[k])
+
+
+def test_union_head_tiled_weights_and_gathered_rows(jet):
+    """The staging copy reads a tiled W as well as a row-major one, and rows
+    read in place from a padded source give the compact call's bits."""
+    wl = wk.union_choice(150, 700, K=(2, 4), d=256, V=5000, seed_offset=3)
+    sc = jet.JetScorer(wl.d, wl.V, wl.N, wl.n_tok)
+    a = args_of(wl)
+    ref = run(sc, a)
+    compare(wl, ref, oracle.score_workload(wl))
+    Wt = sc.tile_weights(a["W"])
+    tiled = run(sc, dict(a, W=Wt))
+    sc.set_weights_layout(0)
+    for k in ref:
+        np.testing.assert_array_equal(tiled[k], ref[k])
+    # rows scattered in a larger source, at every third row
+    L = 3
+    src = torch.zeros((wl.N * L, wl.d), dtype=torch.bfloat16, device="cuda")
+    row_index = torch.arange(wl.N, dtype=torch.int32, device="cuda") * L + 1
+    src[row_index.long()] = a["H"]
+    out = sc.score_sets_gather(src, row_index, a["W"], a["tok_row"], a["tok_ids"], a["cand_offsets"],
+                               a["set_offsets"], a["kind"], wl.T, wl.mode, a["union_ids"])
+    torch.cuda.synchronize()
+    for k in ref:
+        np.testing.assert_array_equal(out[k].cpu().numpy(), ref[k])
+
+
+def test_union_head_status_codes(jet):
+    """The pre-pass performs the restricted checks on this path: a repeated or
+    out-of-range union id, a token outside the union, a multi-token
+    candidate, ids and rows out of range, bad offsets; the context keeps
+    working after each."""
+    wl = wk.union_choice(40, 300, K=(2, 4), d=64, V=2000, seed_offset=4)
+    sc = jet.JetScorer(wl.d, wl.V, wl.N + 8, wl.n_tok + 8)
+    a = args_of(wl)
+    assert uses_union_head(jet, sc, a)
+    assert status(jet, sc, a) == OK
+    u = wl.union_ids.copy(); u[7] = u[3]
+    assert status(jet, sc, args_of(wl, union_ids=dev(u))) == UNION          # repeated id
+    u = wl.union_ids.copy(); u[9] = wl.V
+    assert status(jet, sc, args_of(wl, union_ids=dev(u))) == TOKEN          # id outside [0, V)
+    used = set(wl.tok_ids.tolist())
+    i = [j for j, x in enumerate(wl.union_ids) if int(x) in used][0]
+    u = wl.union_ids.copy(); u[i] = [v for v in range(wl.V) if v not in set(u.tolist())][0]
+    assert status(jet, sc, args_of(wl, union_ids=dev(u))) == UNION          # a candidate token not in U
+    t = wl.tok_ids.copy(); t[2] = wl.V + 5
+    assert status(jet, sc, args_of(wl, tok_ids=dev(t))) == TOKEN
+    r = wl.tok_row.copy(); r[0] = wl.N
+    assert status(jet, sc, args_of(wl, tok_row=dev(r))) == TOKEN
+    co = wl.cand_offsets.copy(); co[-1] += 1
+    assert status(jet, sc, args_of(wl, cand_offsets=dev(co))) == OFFSETS
+    kd = wl.kind.copy(); kd[1] = 9
+    assert status(jet, sc, args_of(wl, kind=dev(kd))) == ARG
+    multi = wk.custom(64, 2000, 6, K=(2, 4), length=(2, 3), seed=21)
+    m = args_of(multi, mode=wk.MODE_RESTRICTED, union_ids=dev(np.arange(2000, dtype=np.int32)))
+    sc2 = jet.JetScorer(64, 2000, multi.N, multi.n_tok)
+    assert status(jet, sc2, m) == MODE                                       # two-token candidates
+    assert status(jet, sc, a) == OK
+    compare(wl, run(sc, a), oracle.score_workload(wl))
+
+
+FORCED = r"""
+import sys
+sys.path.insert(0, {root!r}); sys.path.insert(0, {tests!r})
+import numpy as np, torch
+import oracle, workloads as wk
+import candidate_answer_scoring_gb300 as jet
+from parity import compare
+cases = [wk.union_choice({n_q}, {n_union}, K=(2, 6), d={d}, V={V}, seed_offset={seed})]
+for wl in cases:
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    sc = jet.JetScorer(wl.d, wl.V, wl.N, wl.n_tok)
+    sc.profile(True)
+    out = sc.score_sets(t(wl.H.view(np.int16)).view(torch.bfloat16), t(wl.W.view(np.int16)).view(torch.bfloat16),
+                        t(wl.tok_row), t(wl.tok_ids), t(wl.cand_offsets), t(wl.set_offsets), t(wl.kind), wl.T,
+                        wl.mode, t(wl.union_ids))
+    torch.cuda.synchronize()
+    prof = sc.profile_read()
+    compare(wl, {{k: v.cpu().numpy() for k, v in out.items()}}, oracle.score_workload(wl))
+    print("head", prof["head"]["launches"], "restricted", prof["restricted"]["launches"], "ok")
+"""
+
+
+@pytest.mark.parametrize("env,n_union,n_q,d,V,want_head", [
+    ("0", 600, 200, 256, 8000, False),      # mma.sync kernel on a union it no longer serves by default
+    ("0", 4000, 300, 128, 6000, False),     # ... past its union-logit scratch (recomputed logits)
+    ("1", 26, 300, 128, 3000, True),        # tensor-core head on the 26-code union
+    ("1", 1, 40, 64, 500, True),            # ... and on a one-code union (q = 1, logp = 0)
+])
+def test_forced_projection_path_matches_oracle(env, n_union, n_q, d, V, want_head):
+    code = FORCED.format(root=ROOT, tests=os.path.join(ROOT, "tests"), n_q=n_q, n_union=n_union, d=d, V=V,
+                         seed=n_union + 1)
+    r = subprocess.run([sys.executable, "-c", code], env={**os.environ, "JETSCORE_RESTRICTED_TC": env},
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-4000:]
+    line = [x for x in r.stdout.splitlines() if x.endswith(" ok")]
+    assert len(line) == 1, r.stdout
+    head = int(line[0].split()[1])
+    assert (head > 0) == want_head, line[0]

@@ -430,6 +430,25 @@ def custom(d: int, V: int, n_sets: int, K: Tuple[int, int] = (2, 8), length: Tup
     return _build(f"custom-d{d}-V{V}-s{n_sets}", seed, d, V, W, sets, T, row_mode=row_mode, peak=peak)
 
 
+def union_choice(n_questions: int = 256, n_union: int = 600, K: Tuple[int, int] = (2, 2),
+                 d: int = 2560, V: int = 248320, T: float = T_FITTED, seed_offset: int = 0) -> Workload:
+    """Restricted mode over a larger union of single-token codes: n_union
+    distinct ids drawn once; each question is a set of K ~ U{K[0]..K[1]}
+    distinct codes of the union (binary when K = 2, else choice), one hidden
+    row per question (shared by its codes)."""
+    seed = BASE_SEED + 200 + seed_offset
+    W = gen_W(seed, V, d)
+    rng = _rng(seed, 1)
+    union = np.asarray(_distinct_firsts(rng, V, n_union), np.int32)
+    sets = []
+    for _ in range(n_questions):
+        k = min(int(rng.integers(K[0], K[1] + 1)), n_union)
+        codes = [(int(t),) for t in rng.choice(union, size=k, replace=False)]
+        sets.append(_SetSpec(KIND_BINARY if k == 2 else KIND_CHOICE, codes))
+    wl = _build(f"union{n_union}-d{d}-V{V}-q{n_questions}", seed, d, V, W, sets, 1.0, row_mode="per_key")
+    return wl.with_mode(MODE_RESTRICTED, T, union)
+
+
 NAMED = {
     "tiny": tiny,
     "binary": binary_batch,
