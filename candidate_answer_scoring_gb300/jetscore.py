@@ -347,6 +347,41 @@ class JetScorer:
             raise JetError(rc, "jet_score_sets_host")
         return out
 
+    def bind_call(self, H, W, tok_row, tok_ids, cand_offsets, set_offsets, kind, T: float,
+                  mode: int = JET_MODE_FULL, union_ids=None, out: Optional[Dict[str, torch.Tensor]] = None,
+                  sync: bool = False):
+        """score_sets on device tensors with its checks and argument marshalling
+        done once: returns (call, out), where call() makes only the
+        jet_score_sets_async C call (jet_score_sets with sync=True) on the
+        stream current at bind time, as a C caller holding these buffers would,
+        and raises JetError on a non-zero status.  The tensors must stay alive
+        and unchanged in shape while call is used; their contents may change
+        between calls."""
+        dev = self.device
+        _check_dev(H, "H", dev, _BF16); _check_dev(W, "W", dev, _BF16)
+        for name, t in (("tok_row", tok_row), ("tok_ids", tok_ids), ("cand_offsets", cand_offsets),
+                        ("set_offsets", set_offsets)):
+            _check_dev(t, name, dev, (torch.int32,))
+        _check_dev(kind, "kind", dev, (torch.uint8,))
+        if union_ids is not None:
+            _check_dev(union_ids, "union_ids", dev, (torch.int32,))
+        if out is None:
+            out = self.alloc_outputs(H.shape[0], tok_ids.numel(), cand_offsets.numel() - 1,
+                                     set_offsets.numel() - 1)
+        args, keep = self._set_args(H, W, tok_row, tok_ids, cand_offsets, set_offsets, kind, T, mode, union_ids,
+                                    out)
+        args = tuple(args) + (_stream(dev),)
+        fn = self.lib.jet_score_sets if sync else self.lib.jet_score_sets_async
+        held = (H, W, tok_row, tok_ids, cand_offsets, set_offsets, kind, union_ids, out, keep)
+
+        def call():
+            rc = fn(*args)
+            if rc != JET_OK:
+                raise JetError(rc, "jet_score_sets")
+            return held
+
+        return call, out
+
     def bind_host_call(self, H, W, tok_row, tok_ids, cand_offsets, set_offsets, kind, T: float,
                        mode: int = JET_MODE_FULL, union_ids=None,
                        out: Optional[Dict[str, torch.Tensor]] = None):

@@ -309,6 +309,40 @@ def test_bound_host_call_matches_host_entry(jet):
     compare(b, got, oracle.score_workload(b))
 
 
+def test_bound_device_call_matches_score_sets(jet):
+    """bind_call marshals once; each call() is the bare asynchronous C call on
+    the same device buffers: bit-identical to score_sets in full and
+    restricted mode, new contents written into the inputs are scored, and a
+    device-side rejection surfaces through the synchronous form."""
+    import dataclasses
+    a = wk.custom(128, 1200, 20, K=(2, 6), length=(1, 4), seed=19)
+    r = wk.binary_restricted(base=wk.binary_batch(n_questions=60, random_pairs=True, d=128, V=1200))
+    for wl in (a, r):
+        sc = jet.JetScorer(wl.d, wl.V, wl.N, wl.n_tok)
+        x = to_dev(wl)
+        args = (x["H"], x["W"], x["tok_row"], x["tok_ids"], x["cand_offsets"], x["set_offsets"], x["kind"], wl.T,
+                wl.mode, x["union_ids"])
+        call, out = sc.bind_call(*args)
+        ref = sc.score_sets(*args)
+        call()
+        assert sc.sync_status() == 0
+        for k in OUT_KEYS:
+            assert torch.equal(out[k].view(torch.int32), ref[k].view(torch.int32)), k
+    rng = np.random.default_rng(20)
+    b = dataclasses.replace(a, H=wk.to_bf16_bits(rng.normal(size=a.H.shape).astype(np.float32)))
+    sc = jet.JetScorer(a.d, a.V, a.N, a.n_tok)
+    x = to_dev(a)
+    call, out = sc.bind_call(x["H"], x["W"], x["tok_row"], x["tok_ids"], x["cand_offsets"], x["set_offsets"],
+                             x["kind"], a.T, sync=True)
+    x["H"].copy_(to_dev(b)["H"])   # new rows, same shapes
+    call()
+    compare(b, {k: v.cpu().numpy() for k, v in out.items()}, oracle.score_workload(b))
+    x["tok_ids"][0] = a.V          # rejected by the pre-pass
+    with pytest.raises(jet.JetError) as e:
+        call()
+    assert e.value.status == -2
+
+
 def test_host_entry_restricted_subset_and_errors(jet):
     """The host entry packs the index arrays into one copy in and the requested
     outputs (behind the status words) into one copy out: restricted mode, a
