@@ -713,8 +713,8 @@ def op_arm(args):
             Wt = sc.tile_weights(W_dev) if args.w_layout == "tiled" else W_dev
             x = [t(a) for a in (wl.tok_row, wl.tok_ids, wl.cand_offsets, wl.set_offsets, wl.kind, wl.union_ids)]
             H = t(wl.H.view(np.int16)).view(torch.bfloat16)
-            o = sc.alloc_outputs(wl.N, wl.n_tok, wl.n_cand, wl.n_sets)
-            fn = lambda: sc.score_sets(H, Wt, x[0], x[1], x[2], x[3], x[4], wl.T, wl.mode, x[5], out=o, sync=False)
+            # the bare C call, arguments marshalled once (as a C caller holding these buffers)
+            fn = sc.bind_call(H, Wt, x[0], x[1], x[2], x[3], x[4], wl.T, wl.mode, x[5])[0]
             ms = time_op(fn, K, W)
             sc.profile(True)
             time_op(fn, K, 0)

@@ -77,7 +77,7 @@ bool head_use_dynamic(const Plan& p) {
 // copy and used as the vocabulary) for unions of at least this many codes;
 // smaller unions take the two-launch mma.sync path.  JETSCORE_RESTRICTED_TC=0/1
 // forces a path (diagnostics; 1 applies wherever the staging copy fits).
-constexpr int RESTRICTED_TC_MIN_UNION = 256;
+constexpr int RESTRICTED_TC_MIN_UNION = 192;
 
 bool restricted_use_tc(int n_union, int staging_rows) {
   static int env = -2;

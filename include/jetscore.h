@@ -172,7 +172,7 @@ typedef struct {
  *       JET_MODE_RESTRICTED: normalise over union_ids[n_union] (distinct ids,
  *       1 <= n_union <= JET_MAX_UNION); every candidate is one token of the
  *       union (PARALLEL_SCORING page, "Execution" step 5).  union_ids is ignored
- *       in full mode.  Unions of fewer than 256 codes are projected by a small
+ *       in full mode.  Unions of fewer than 192 codes are projected by a small
  *       tensor-core kernel (mma.sync); larger ones are copied into the
  *       context's staging rows and projected by the full-vocabulary tcgen05
  *       head with the union as its vocabulary (JETSCORE_RESTRICTED_TC=0|1

@@ -1,4 +1,4 @@
-"""Restricted mode over larger unions: from 256 codes the union's rows of W are
+"""Restricted mode over larger unions: from 192 codes the union's rows of W are
 staged and the tcgen05 head runs with the union as its vocabulary (PARALLEL_
 SCORING page, "Execution" steps 5-6: project the final hidden states onto the
 gathered union, softmax over each field's candidates).  Parity with the oracle
@@ -68,7 +68,7 @@ def uses_union_head(jet, sc, a):
 
 
 @pytest.mark.parametrize("n_union,K,d,V,n_q", [
-    (256, (2, 2), 128, 3000, 300),      # the smallest union on the tensor-core head; 2 row tiles
+    (192, (2, 2), 128, 3000, 300),      # the smallest union on the tensor-core head; 2 row tiles
     (600, (2, 9), 512, 20000, 120),     # a ragged union tile (600 = 2 x 256 + 88)
     (4096, (2, 6), 256, 9000, 500),     # the largest accepted union
 ])
