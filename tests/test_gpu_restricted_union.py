@@ -213,3 +213,19 @@ def test_forced_projection_path_matches_oracle(env, n_union, n_q, d, V, want_hea
     assert len(line) == 1, r.stdout
     head = int(line[0].split()[1])
     assert (head > 0) == want_head, line[0]
+
+
+@pytest.mark.parametrize("n_union", [600, 4096])
+def test_union_head_full_size_binary_shape(jet, n_union):
+    """The benchmark's restricted configuration at full size: 256 questions of
+    the binary batch's shape (d = 2560, V = 248320), each a pair of codes
+    from the union; W in the tiled layout and the bare C call, as timed."""
+    wl = wk.union_choice(256, n_union)
+    sc = jet.JetScorer(wl.d, wl.V, wl.N, wl.n_tok)
+    a = args_of(wl)
+    Wt = sc.tile_weights(a["W"])
+    call, out = sc.bind_call(a["H"], Wt, a["tok_row"], a["tok_ids"], a["cand_offsets"], a["set_offsets"],
+                             a["kind"], wl.T, wl.mode, a["union_ids"], sync=True)
+    call()
+    gpu = {k: v.cpu().numpy() for k, v in out.items()}
+    compare(wl, gpu, oracle.score_workload(wl))
