@@ -165,10 +165,16 @@ def job_throughput(tokens_per_step, steps, world, ms):
     return world * tokens_per_step * steps / (ms / 1e3)
 
 
+_GENERATED = {}
+
+
 def make_workload(name, rank=0):
     import workloads as wk
-    gen = getattr(wk, WORKLOADS[name][0])
-    base = gen()
+    gen_name = WORKLOADS[name][0]
+    if gen_name not in _GENERATED:         # the binary batch serves three workloads: generate it once
+        _GENERATED.clear()
+        _GENERATED[gen_name] = getattr(wk, gen_name)()
+    base = _GENERATED[gen_name]
     steps = []
     for mode in WORKLOADS[name][1]:
         if mode == "full":

@@ -139,7 +139,8 @@ def test_many_waves_with_an_odd_number_of_k_blocks():
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
     sc = jet_mod.JetScorer(d, V, n, n)
     info = sc.plan_info(n)
-    assert info["tile_rows"] == 256 and info["units"] > info["ctas"] // 2, info
+    if "JETSCORE_HEAD_PAIR" not in os.environ:   # a suite-wide variant override picks the head itself
+        assert info["tile_rows"] == 256 and info["units"] > info["ctas"] // 2, info
     lp, lse = sc.score_tokens(dev(H.view(np.int16)).view(torch.bfloat16), dev(W.view(np.int16)).view(torch.bfloat16),
                               dev(tok), want_lse=True)
     torch.cuda.synchronize()

@@ -3,6 +3,8 @@ holds W's elements where the header says, and every path that reads W — the
 full-vocabulary head (one-CTA and paired), the restricted head, and the
 restricted set kernel's recomputation when the union logits do not fit the
 scratch — gives the same bits as with row-major W."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -109,7 +111,8 @@ def test_tiled_weights_in_score_tokens_and_many_waves(jet):
     Hd = dev(H.view(np.int16)).view(torch.bfloat16)
     sc = jet.JetScorer(d, V, n, n)
     info = sc.plan_info(n)
-    assert info["tile_rows"] == 256 and info["units"] > info["ctas"] // 2, info
+    if "JETSCORE_HEAD_PAIR" not in os.environ:   # a suite-wide variant override picks the head itself
+        assert info["tile_rows"] == 256 and info["units"] > info["ctas"] // 2, info
     lp_row, lse_row = sc.score_tokens(Hd, Wd, dev(tok), want_lse=True)
     Wt = sc.tile_weights(Wd)
     lp_t, lse_t = sc.score_tokens(Hd, Wt, dev(tok), want_lse=True)
