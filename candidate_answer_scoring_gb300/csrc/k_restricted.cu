@@ -9,8 +9,10 @@
 // The set rules then run unchanged; within a set sharing one row, lse_U
 // cancels and q = softmax(z / T) over the set's codes (step 6).
 //
-// The work is tiny (|U| is tens of codes) and latency-bound, so the path is
-// two launches with few dependent memory round trips each:
+// For unions below 192 codes (answer codes A..Z are 26) the work is tiny and
+// latency-bound, so the path is two launches with few dependent memory round
+// trips each; larger unions are staged by union_rows_kernel (end of this
+// file) and projected by the full-vocabulary tcgen05 head instead:
 //
 //  1. restricted_head_kernel: z = H U^T is a small dense contraction, run on
 //     the tensor cores with mma.sync (m16n8k16, bf16 in, fp32 accumulate).
