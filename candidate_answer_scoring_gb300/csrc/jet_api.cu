@@ -110,6 +110,7 @@ constexpr int UNITS_PER_SM_CAP = 64;   // bound on schedule units (partials work
 constexpr size_t ZU_FLOATS_PER_ROW = 128;
 constexpr size_t ZU_FLOATS_MIN = size_t(1) << 20;
 constexpr size_t IO_HEAD = 64;   // bytes of the error words at the front of the output block
+constexpr int STATUS_RING = 4096;   // per-call status words of jet_score_sets_host_async between waits
 
 template <class T>
 cudaError_t dalloc(T** p, size_t n) {
@@ -153,6 +154,17 @@ struct jet_ctx {
   uint8_t *io_dev = nullptr, *h_out = nullptr;  // device / pinned host: [IO_HEAD error words][outputs]
   size_t in_cap = 0, out_cap = 0;
   int* h_err = nullptr;   // pinned
+  // jet_score_sets_host_async: the second staging slot (slot 0 is stH/d_in),
+  // the copy stream, per-slot events, and the per-call status words (pinned)
+  uint16_t* stH2 = nullptr;
+  uint8_t* d_in2 = nullptr;
+  cudaStream_t copy_st = nullptr;
+  cudaEvent_t ev_copied[2] = {nullptr, nullptr};   // slot's inputs are on the device
+  cudaEvent_t ev_free[2] = {nullptr, nullptr};     // the kernels reading the slot are done
+  int* h_status = nullptr;                         // [STATUS_RING]
+  int n_async = 0;                                 // calls since the last jet_host_wait
+  int async_err = 0;                               // first status seen by an implicit wait
+  unsigned long long async_calls = 0;              // slot of the next call = its parity
   // row deduplication workspace
   unsigned long long *dd_hash = nullptr, *dd_keys = nullptr;
   int *dd_vals = nullptr, *dd_rep = nullptr, *dd_rank = nullptr, *dd_tiles = nullptr;
@@ -552,6 +564,14 @@ void jet_destroy(jet_ctx* c) {
     if (p) cudaFree(p);
   for (auto& v : c->ev)
     for (cudaEvent_t e : v) cudaEventDestroy(e);
+  for (int i = 0; i < 2; ++i) {
+    if (c->ev_copied[i]) cudaEventDestroy(c->ev_copied[i]);
+    if (c->ev_free[i]) cudaEventDestroy(c->ev_free[i]);
+  }
+  if (c->copy_st) cudaStreamDestroy(c->copy_st);
+  if (c->stH2) cudaFree(c->stH2);
+  if (c->d_in2) cudaFree(c->d_in2);
+  if (c->h_status) cudaFreeHost(c->h_status);
   if (c->h_err) cudaFreeHost(c->h_err);
   if (c->h_in) cudaFreeHost(c->h_in);
   if (c->h_out) cudaFreeHost(c->h_out);
@@ -921,6 +941,142 @@ int jet_score_sets_host(jet_ctx* c, const void* H, const void* W, int n_rows, co
   unpack(h.expected, dev.expected, (size_t)n_sets * 4);
   unpack(h.confidence, dev.confidence, (size_t)n_sets * 4);
   unpack(h.mass, dev.mass, (size_t)n_sets * 4);
+  return status;
+}
+
+}  // extern "C"
+
+namespace {
+
+// Second staging slot, copy stream and events of jet_score_sets_host_async,
+// made on the first call (each piece once, so a failed set-up can be retried).
+int host_async_setup(jet_ctx* c) {
+  if (c->copy_st) return JET_OK;
+  cudaError_t e = cudaSuccess;
+  auto A = [&](cudaError_t r) { if (e == cudaSuccess) e = r; };
+  if (!c->stH2) A(dalloc(&c->stH2, (size_t)c->max_rows * c->d));
+  if (!c->d_in2) A(dalloc(&c->d_in2, c->in_cap));
+  if (!c->h_status) A(cudaMallocHost(reinterpret_cast<void**>(&c->h_status), STATUS_RING * sizeof(int)));
+  for (int i = 0; i < 2; ++i) {
+    if (!c->ev_copied[i]) A(cudaEventCreateWithFlags(&c->ev_copied[i], cudaEventDisableTiming));
+    if (!c->ev_free[i]) A(cudaEventCreateWithFlags(&c->ev_free[i], cudaEventDisableTiming));
+  }
+  if (e == cudaSuccess) A(cudaStreamCreateWithFlags(&c->copy_st, cudaStreamNonBlocking));
+  return e == cudaSuccess ? JET_OK : JET_ERR_CUDA;
+}
+
+// Waits for `st` and folds the statuses of the calls since the last wait into
+// async_err (first non-zero wins).
+int host_async_drain(jet_ctx* c, cudaStream_t st) {
+  if (cudaStreamSynchronize(st) != cudaSuccess) return JET_ERR_CUDA;
+  for (int i = 0; i < c->n_async && c->async_err == 0; ++i) c->async_err = c->h_status[i];
+  c->n_async = 0;
+  return JET_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int jet_score_sets_host_async(jet_ctx* c, const void* H, const void* W, int n_rows, const int32_t* tok_row,
+                              const int32_t* tok_ids, int n_tok, const int32_t* cand_offsets, int n_cand,
+                              const int32_t* set_offsets, const uint8_t* kind, int n_sets, float T, int mode,
+                              const int32_t* union_ids, int n_union, const jet_set_out* out_host, void* stream) {
+  int rc = check_sets_args(c, H, W, n_rows, tok_row, tok_ids, n_tok, cand_offsets, n_cand, set_offsets, kind,
+                           n_sets, T, mode, union_ids, n_union);
+  if (rc != JET_OK || n_tok == 0) return rc;
+  DeviceGuard g(c->device);
+  if (!g.ok) return JET_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  rc = host_async_setup(c);
+  if (rc != JET_OK) return rc;
+  if (c->n_async == STATUS_RING && host_async_drain(c, st) != JET_OK) return JET_ERR_CUDA;
+
+  // inputs into this call's slot, on the copy stream, once the kernels that
+  // last read the slot (two calls back) are done
+  const int slot = (int)(c->async_calls & 1);
+  uint16_t* stH = slot ? c->stH2 : c->stH;
+  uint8_t* din = slot ? c->d_in2 : c->d_in;
+  cudaStream_t cs = c->copy_st;
+  bool ok = cudaStreamWaitEvent(cs, c->ev_free[slot], 0) == cudaSuccess;
+  size_t off = 0;
+  auto put = [&](const void* src, size_t bytes) -> const void* {
+    uint8_t* dst = din + off;
+    off += (bytes + 15) & ~size_t(15);
+    ok = ok && cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, cs) == cudaSuccess;
+    return dst;
+  };
+  const int32_t* d_row = static_cast<const int32_t*>(put(tok_row, (size_t)n_tok * 4));
+  const int32_t* d_tok = static_cast<const int32_t*>(put(tok_ids, (size_t)n_tok * 4));
+  const int32_t* d_co = static_cast<const int32_t*>(put(cand_offsets, (size_t)(n_cand + 1) * 4));
+  const int32_t* d_so = static_cast<const int32_t*>(put(set_offsets, (size_t)(n_sets + 1) * 4));
+  const uint8_t* d_kind = static_cast<const uint8_t*>(put(kind, (size_t)n_sets));
+  const int32_t* d_union =
+      mode == JET_MODE_RESTRICTED ? static_cast<const int32_t*>(put(union_ids, (size_t)n_union * 4)) : nullptr;
+  ok = ok && cudaMemcpyAsync(stH, H, (size_t)n_rows * c->d * 2, cudaMemcpyHostToDevice, cs) == cudaSuccess;
+  ok = ok && cudaEventRecord(c->ev_copied[slot], cs) == cudaSuccess;
+  ok = ok && cudaStreamWaitEvent(st, c->ev_copied[slot], 0) == cudaSuccess;
+  if (!ok) return JET_ERR_CUDA;
+  c->async_calls += 1;
+
+  // outputs: written by the kernels into the output block (in stream order,
+  // so the next call's kernels come after these copies), copied to the caller
+  jet_set_out h;
+  std::memset(&h, 0, sizeof h);
+  if (out_host) h = *out_host;
+  jet_set_out dev;
+  std::memset(&dev, 0, sizeof dev);
+  size_t out_off = IO_HEAD;
+  auto place = [&](void* host_ptr, size_t bytes) -> uint8_t* {
+    if (!host_ptr) return nullptr;
+    uint8_t* p = c->io_dev + out_off;
+    out_off += (bytes + 15) & ~size_t(15);
+    return p;
+  };
+  dev.logp = reinterpret_cast<float*>(place(h.logp, (size_t)n_tok * 4));
+  dev.lse = reinterpret_cast<float*>(place(h.lse, (size_t)n_rows * 4));
+  dev.s = reinterpret_cast<float*>(place(h.s, (size_t)n_cand * 4));
+  dev.q = reinterpret_cast<float*>(place(h.q, (size_t)n_cand * 4));
+  dev.q_equiv = reinterpret_cast<float*>(place(h.q_equiv, (size_t)n_cand * 4));
+  dev.decision = reinterpret_cast<int32_t*>(place(h.decision, (size_t)n_sets * 4));
+  dev.expected = reinterpret_cast<float*>(place(h.expected, (size_t)n_sets * 4));
+  dev.confidence = reinterpret_cast<float*>(place(h.confidence, (size_t)n_sets * 4));
+  dev.mass = reinterpret_cast<float*>(place(h.mass, (size_t)n_sets * 4));
+  rc = score_sets_enqueue(c, stH, W, n_rows, d_row, d_tok, n_tok, d_co, n_cand, d_so, d_kind, n_sets, T, mode,
+                          d_union, n_union, &dev, st);
+  if (rc != JET_OK) {
+    cudaStreamSynchronize(st);
+    return rc;
+  }
+  ok = cudaEventRecord(c->ev_free[slot], st) == cudaSuccess;
+  auto get = [&](void* host_ptr, const void* dev_ptr, size_t bytes) {
+    if (host_ptr) ok = ok && cudaMemcpyAsync(host_ptr, dev_ptr, bytes, cudaMemcpyDeviceToHost, st) == cudaSuccess;
+  };
+  get(h.logp, dev.logp, (size_t)n_tok * 4);
+  get(h.lse, dev.lse, (size_t)n_rows * 4);
+  get(h.s, dev.s, (size_t)n_cand * 4);
+  get(h.q, dev.q, (size_t)n_cand * 4);
+  get(h.q_equiv, dev.q_equiv, (size_t)n_cand * 4);
+  get(h.decision, dev.decision, (size_t)n_sets * 4);
+  get(h.expected, dev.expected, (size_t)n_sets * 4);
+  get(h.confidence, dev.confidence, (size_t)n_sets * 4);
+  get(h.mass, dev.mass, (size_t)n_sets * 4);
+  get(c->h_status + c->n_async, c->err, sizeof(int));
+  c->n_async += 1;
+  if (!ok) {
+    cudaStreamSynchronize(st);
+    return JET_ERR_CUDA;
+  }
+  return JET_OK;
+}
+
+int jet_host_wait(jet_ctx* c, void* stream) {
+  if (!c) return JET_ERR_ARG;
+  DeviceGuard g(c->device);
+  if (!g.ok) return JET_ERR_CUDA;
+  if (host_async_drain(c, static_cast<cudaStream_t>(stream)) != JET_OK) return JET_ERR_CUDA;
+  const int status = c->async_err;
+  c->async_err = 0;
   return status;
 }
 

@@ -69,8 +69,9 @@ def load() -> C.CDLL:
     lib.jet_status_string.restype = C.c_char_p
     lib.jet_score_tokens.argtypes = [P, P, P, P, I, P, P, P]
     sets_sig = [P, P, P, I, P, P, I, P, I, P, P, I, F, I, P, I, C.POINTER(_SetOut), P]
-    for name in ("jet_score_sets", "jet_score_sets_async", "jet_score_sets_host"):
+    for name in ("jet_score_sets", "jet_score_sets_async", "jet_score_sets_host", "jet_score_sets_host_async"):
         getattr(lib, name).argtypes = sets_sig
+    lib.jet_host_wait.argtypes = [P, P]
     lib.jet_tiled_weights_bytes.argtypes = [P]
     lib.jet_tiled_weights_bytes.restype = C.c_size_t
     lib.jet_tile_weights.argtypes = [P, P, P, P]
@@ -384,13 +385,16 @@ class JetScorer:
 
     def bind_host_call(self, H, W, tok_row, tok_ids, cand_offsets, set_offsets, kind, T: float,
                        mode: int = JET_MODE_FULL, union_ids=None,
-                       out: Optional[Dict[str, torch.Tensor]] = None):
+                       out: Optional[Dict[str, torch.Tensor]] = None, pipelined: bool = False):
         """score_sets_host with its checks and argument marshalling done once:
         returns (call, out), where call() makes only the jet_score_sets_host
         C call on the current stream (as a C caller holding these buffers
         would) and raises JetError on a non-zero status.  The tensors must stay
         alive and unchanged in shape while call is used; their contents may
-        change between calls."""
+        change between calls.  With pipelined=True the call is
+        jet_score_sets_host_async: it returns after enqueueing (the host
+        tensors must be pinned), consecutive calls overlap their input copies
+        with the previous call's kernels, and host_wait() collects them."""
         _check_dev(W, "W", self.device, _BF16)
         cpu = torch.device("cpu")
         _check_dev(H, "H", cpu, _BF16)
@@ -409,7 +413,7 @@ class JetScorer:
         args, keep = self._set_args(H, W, tok_row, tok_ids, cand_offsets, set_offsets, kind, T, mode, union_ids,
                                     out)
         args = tuple(args) + (_stream(self.device),)
-        fn = self.lib.jet_score_sets_host
+        fn = self.lib.jet_score_sets_host_async if pipelined else self.lib.jet_score_sets_host
         held = (H, W, tok_row, tok_ids, cand_offsets, set_offsets, kind, union_ids, out, keep)
 
         def call():
@@ -419,3 +423,9 @@ class JetScorer:
             return held
 
         return call, out
+
+    def host_wait(self) -> int:
+        """Wait for the pipelined host calls (bind_host_call(pipelined=True))
+        enqueued since the last wait on the current stream; returns the first
+        non-zero device status among them (0 if none)."""
+        return int(self.lib.jet_host_wait(self._h, _stream(self.device)))

@@ -250,6 +250,35 @@ int jet_score_sets_host(jet_ctx *ctx, const void *H_bf16_host, const void *W_bf1
                         void *cuda_stream);
 
 /*
+ * jet_score_sets_host_async / jet_host_wait: jet_score_sets_host for a stream
+ * of batches, returning after enqueueing so that consecutive calls overlap:
+ * each call copies its inputs into one of two device staging slots on the
+ * context's own copy stream (the copy of batch k+1 runs while the kernels of
+ * batch k run on `cuda_stream`), then enqueues the kernels and the copies of
+ * the requested outputs (and of the call's status) back into the caller's
+ * host buffers on `cuda_stream`.  Arguments as jet_score_sets_host, except:
+ *   - every host buffer (H, the index arrays, union_ids, the members of
+ *     *out_host) must be page-locked (cudaHostAlloc / cudaHostRegister);
+ *   - inputs must stay unmodified, and outputs unread, until jet_host_wait
+ *     returns; every call between two waits uses the same `cuda_stream`, and
+ *     no other call uses the context until the wait (the slots are its
+ *     staging buffers).
+ * The first call allocates the second staging slot (max_rows x d bf16 plus
+ * the index arrays) and creates the copy stream.  Host checks fail at once,
+ * with nothing enqueued; device-side statuses are collected by the wait.
+ * After 4096 calls without a wait, a call waits for the earlier ones first.
+ * jet_host_wait: waits for `cuda_stream` and returns the first non-zero status
+ * of the calls enqueued since the previous wait (JET_OK if none).
+ */
+int jet_score_sets_host_async(jet_ctx *ctx, const void *H_bf16_host, const void *W_bf16_dev, int n_rows,
+                              const int32_t *tok_row, const int32_t *tok_ids, int n_tok,
+                              const int32_t *cand_offsets, int n_cand, const int32_t *set_offsets,
+                              const uint8_t *kind, int n_sets, float T, int mode,
+                              const int32_t *union_ids, int n_union, const jet_set_out *out_host,
+                              void *cuda_stream);
+int jet_host_wait(jet_ctx *ctx, void *cuda_stream);
+
+/*
  * jet_dedup_rows: project each distinct predictor state once -- the
  * candidate-preserving readout of FastJEV (section 3.3: project each required
  * predictor node once, normalise over the full vocabulary, gather the token

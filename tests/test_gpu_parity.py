@@ -309,6 +309,51 @@ def test_bound_host_call_matches_host_entry(jet):
     compare(b, got, oracle.score_workload(b))
 
 
+def test_pipelined_host_calls_match_host_entry(jet):
+    """jet_score_sets_host_async: six calls alternating two batches (two
+    staging slots, so each slot is reused while the other call's kernels may
+    run), each into its own pinned outputs, equal the synchronous host entry
+    bit for bit after one jet_host_wait; a device-side rejection among them is
+    returned by the wait, and the context works afterwards."""
+    import dataclasses
+    a = wk.custom(128, 1200, 20, K=(2, 6), length=(1, 4), seed=23)
+    rng = np.random.default_rng(24)
+    b = dataclasses.replace(a, H=wk.to_bf16_bits(rng.normal(size=a.H.shape).astype(np.float32)))
+    sc = jet.JetScorer(a.d, a.V, a.N, a.n_tok)
+    W = to_dev(a)["W"]
+    pin = lambda x: torch.from_numpy(np.ascontiguousarray(x)).pin_memory()
+    batches = []
+    for wl in (a, b):
+        args = (pin(wl.H.view(np.int16)).view(torch.bfloat16), W, pin(wl.tok_row), pin(wl.tok_ids),
+                pin(wl.cand_offsets), pin(wl.set_offsets), pin(wl.kind), wl.T)
+        batches.append((args, sc.score_sets_host(*args)))
+    calls = []
+    for i in range(6):
+        args, _ = batches[i % 2]
+        calls.append(sc.bind_host_call(*args, pipelined=True))
+    for call, _ in calls:
+        call()
+    assert sc.host_wait() == 0
+    for i, (_, out) in enumerate(calls):
+        ref = batches[i % 2][1]
+        for k in OUT_KEYS:
+            assert np.array_equal(out[k].numpy().view(np.uint32), ref[k].numpy().view(np.uint32)), (i, k)
+    # a rejected call among valid ones
+    args, _ = batches[0]
+    bad_ids = args[3].clone().pin_memory()
+    bad_ids[1] = a.V
+    bad, _ = sc.bind_host_call(args[0], W, args[2], bad_ids, *args[4:], pipelined=True)
+    calls[0][0]()
+    bad()
+    calls[1][0]()
+    assert sc.host_wait() == -2
+    calls[2][0]()
+    calls[3][0]()
+    assert sc.host_wait() == 0
+    for k in OUT_KEYS:
+        assert np.array_equal(calls[3][1][k].numpy().view(np.uint32), batches[1][1][k].numpy().view(np.uint32)), k
+
+
 def test_bound_device_call_matches_score_sets(jet):
     """bind_call marshals once; each call() is the bare asynchronous C call on
     the same device buffers: bit-identical to score_sets in full and
