@@ -18,6 +18,7 @@ namespace {
 
 constexpr int PREP_THREADS = 1024;
 constexpr int PREP_SMEM_ROWS = 6144;   // per-row counters in shared memory up to this many rows
+constexpr int PREP_BATCH = 4;          // independent union lookups in flight per thread (restricted mode)
 
 __device__ __forceinline__ int row_of(const PrepArgs& a, int j) {
   return a.tok_row ? a.tok_row[j] : j;
@@ -53,25 +54,51 @@ __global__ void __launch_bounds__(PREP_THREADS) prep_kernel(PrepArgs a) {
   __syncthreads();
 
   // scored tokens: id in [0, V), row in [0, n_rows); is tok_row non-decreasing?
-  // Restricted mode: the id's union position (a map entry is trusted only
-  // where union_ids agrees, so entries left by earlier calls are harmless).
   for (int j = tid; j < a.n_tok; j += nth) {
     const int t = a.tok_ids[j], r = row_of(a, j);
-    if (t < 0 || t >= a.V || r < 0 || r >= a.n_rows) {
-      set_error(err, JET_ERR_TOKEN_RANGE, j);
-    } else if (a.union_ids) {
-      const int pos = a.umap[t];
-      if (pos < 0 || pos >= a.n_union || a.union_ids[pos] != t) set_error(err, JET_ERR_NOT_IN_UNION, j);
-    }
+    if (t < 0 || t >= a.V || r < 0 || r >= a.n_rows) set_error(err, JET_ERR_TOKEN_RANGE, j);
     if (!identity && j > 0 && a.tok_row[j - 1] > r) s_unsorted = 1;
   }
-
-  // restricted mode: union ids in [0, V) and distinct (a repeated id keeps
-  // one map position, so another of its positions does not map back)
-  for (int u = tid; u < (a.union_ids ? a.n_union : 0); u += nth) {
-    const int t = a.union_ids[u];
-    if (t < 0 || t >= a.V) set_error(err, JET_ERR_TOKEN_RANGE, u);
-    else if (a.umap[t] != u) set_error(err, JET_ERR_NOT_IN_UNION, u);
+  if (a.union_ids) {
+    // Restricted mode: each token's union position (a map entry is trusted
+    // only where union_ids agrees, so entries left by earlier calls are
+    // harmless), and the union ids in [0, V) and distinct (a repeated id
+    // keeps one map position, so another of its positions does not map
+    // back).  PREP_BATCH independent lookups in flight per thread.
+    for (int j0 = tid; j0 < a.n_tok; j0 += nth * PREP_BATCH) {
+      int t[PREP_BATCH], pos[PREP_BATCH];
+#pragma unroll
+      for (int i = 0; i < PREP_BATCH; ++i) {
+        const int j = j0 + i * nth;
+        t[i] = j < a.n_tok ? a.tok_ids[j] : -1;
+      }
+#pragma unroll
+      for (int i = 0; i < PREP_BATCH; ++i) pos[i] = (t[i] >= 0 && t[i] < a.V) ? a.umap[t[i]] : -1;
+#pragma unroll
+      for (int i = 0; i < PREP_BATCH; ++i) {
+        const int j = j0 + i * nth;
+        if (t[i] < 0 || t[i] >= a.V) continue;          // out of range: reported above
+        if (pos[i] < 0 || pos[i] >= a.n_union || a.union_ids[pos[i]] != t[i])
+          set_error(err, JET_ERR_NOT_IN_UNION, j);
+      }
+    }
+    for (int u0 = tid; u0 < a.n_union; u0 += nth * PREP_BATCH) {
+      int t[PREP_BATCH], m[PREP_BATCH];
+#pragma unroll
+      for (int i = 0; i < PREP_BATCH; ++i) {
+        const int u = u0 + i * nth;
+        t[i] = u < a.n_union ? a.union_ids[u] : 0;
+      }
+#pragma unroll
+      for (int i = 0; i < PREP_BATCH; ++i) m[i] = (t[i] >= 0 && t[i] < a.V) ? a.umap[t[i]] : -1;
+#pragma unroll
+      for (int i = 0; i < PREP_BATCH; ++i) {
+        const int u = u0 + i * nth;
+        if (u >= a.n_union) continue;
+        if (t[i] < 0 || t[i] >= a.V) set_error(err, JET_ERR_TOKEN_RANGE, u);
+        else if (m[i] != u) set_error(err, JET_ERR_NOT_IN_UNION, u);
+      }
+    }
   }
 
   // gathered rows: every index within the source array

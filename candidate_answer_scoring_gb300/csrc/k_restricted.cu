@@ -53,6 +53,7 @@ constexpr int RT_UNROLL = 3;                  // 32-wide k chunks with loads in 
 constexpr int RT_SPLIT = 4;                   // CTAs of a cluster splitting d for one 16-row tile
 constexpr int DR_BATCH = 10;                  // 16-byte vectors in flight per lane (warp dot product)
 constexpr int RS_WARPS = 8;                   // sets per CTA of the set kernel
+constexpr int UR_BATCH = 8;                   // 16-byte loads in flight per lane when staging union rows
 
 __device__ __forceinline__ float dot_bf16x8(uint4 h, uint4 w, float acc) {
   const __nv_bfloat162* hp = reinterpret_cast<const __nv_bfloat162*>(&h);
@@ -490,7 +491,15 @@ __global__ void __launch_bounds__(256) union_rows_kernel(const uint4* W, int V, 
     }
     if (lane == 0) umap[t] = u;
     const size_t wb = w_row_base(t, d, tiled);
-    for (int k = lane; k < nvec; k += 32) o[k] = W[w_vec(wb, k, tiled)];
+    for (int k0 = lane; k0 < nvec; k0 += 32 * UR_BATCH) {   // UR_BATCH loads in flight per lane
+      uint4 v[UR_BATCH];
+#pragma unroll
+      for (int j = 0; j < UR_BATCH; ++j)
+        if (k0 + 32 * j < nvec) v[j] = W[w_vec(wb, k0 + 32 * j, tiled)];
+#pragma unroll
+      for (int j = 0; j < UR_BATCH; ++j)
+        if (k0 + 32 * j < nvec) o[k0 + 32 * j] = v[j];
+    }
   }
 }
 
