@@ -238,3 +238,24 @@ def test_union_head_full_size_binary_shape(jet, n_union):
     call()
     gpu = {k: v.cpu().numpy() for k, v in out.items()}
     compare(wl, gpu, oracle.score_workload(wl))
+
+
+def test_union_head_through_host_entries(jet):
+    """The host-buffer entries stage union_ids with the other index arrays:
+    jet_score_sets_host and the pipelined jet_score_sets_host_async give the
+    device call's bits for a 300-code union."""
+    wl = wk.union_choice(80, 300, K=(2, 5), d=128, V=3000, seed_offset=8)
+    sc = jet.JetScorer(wl.d, wl.V, wl.N, wl.n_tok)
+    a = args_of(wl)
+    ref = run(sc, a)
+    pin = lambda x: torch.from_numpy(np.ascontiguousarray(x)).pin_memory()
+    hargs = (pin(wl.H.view(np.int16)).view(torch.bfloat16), a["W"], pin(wl.tok_row), pin(wl.tok_ids),
+             pin(wl.cand_offsets), pin(wl.set_offsets), pin(wl.kind), wl.T, wl.mode, pin(wl.union_ids))
+    host = sc.score_sets_host(*hargs)
+    calls = [sc.bind_host_call(*hargs, pipelined=True) for _ in range(3)]
+    for call, _ in calls:
+        call()
+    assert sc.host_wait() == 0
+    for got in [host] + [out for _, out in calls]:
+        for k in ref:
+            assert np.array_equal(got[k].numpy().view(np.uint32), ref[k].view(np.uint32)), k
