@@ -8,8 +8,10 @@ tcgen05 head, split merge, set rules.  The line's ``per_config`` block times
 the other workloads the same way: the binary batch (256 questions, d=2560,
 V=248320) in full-vocabulary mode, in restricted mode over its 26-code union
 (latency-bound: reported, not a roofline target), and both passes in one step;
-the multi-token choice batch and the wide-schema batch.  The metric is scored
-candidate tokens per second (of the first pass where a step holds two).
+the multi-token choice batch, the wide-schema batch, and the large batch with
+each distinct hidden row projected once (the row-dedup pass inside the step).
+The metric is scored candidate tokens per second (of the first pass where a
+step holds two).
 
 Printed: one JSON line (rank 0).  Timing: CUDA events on the launching stream,
 after warm-up, synchronised on both sides; W (0.8-1.3 GB) is larger than L2, so
@@ -18,7 +20,7 @@ times come from event pairs the library records around its own launches.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
                   [--workload large|binary|multitoken|wideschema|tiny]
-                  [--per-config binary,binary-restricted,binary-both,multitoken,wideschema|none]
+                  [--per-config binary,binary-restricted,binary-both,multitoken,wideschema,large-dedup|none]
 """
 import argparse
 import hashlib
@@ -53,6 +55,9 @@ WORKLOADS = {
                    "wide schema: 16 requests x 32 fields, enum K 2-26 / ordinal K=5, d=2560, V=248320, T=2.179"),
     "large": ("large_choice", ("full",), 40,
               "large choice: 16 requests x K=64, 8-32 tokens, d=4096, V=152064, T=1"),
+    "large-dedup": ("large_choice", ("full",), 40,
+                    "large choice: 16 requests x K=64, 8-32 tokens, d=4096, V=152064, T=1; each distinct hidden "
+                    "row projected once (jet_dedup_rows inside the step)"),
     "tiny": ("tiny", ("full",), 2000, "tiny: d=64, V=1000, 3 sets"),
 }
 
@@ -171,8 +176,7 @@ _GENERATED = {}
 def make_workload(name, rank=0):
     import workloads as wk
     gen_name = WORKLOADS[name][0]
-    if gen_name not in _GENERATED:         # the binary batch serves three workloads: generate it once
-        _GENERATED.clear()
+    if gen_name not in _GENERATED:         # a batch serving several workloads is generated once
         _GENERATED[gen_name] = getattr(wk, gen_name)()
     base = _GENERATED[gen_name]
     steps = []
@@ -313,6 +317,7 @@ def measure_workload(name, args, dev, world, peaks, K, W, keep=False):
     import candidate_answer_scoring_gb300 as jet
 
     wl, steps_wl = make_workload(name)
+    dedup = bool(args.dedup) or name.endswith("-dedup")
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
     Wd = t(wl.W.view(np.int16)).view(torch.bfloat16)
     ins = []
@@ -342,7 +347,7 @@ def measure_workload(name, args, dev, world, peaks, K, W, keep=False):
             x["row_index"] = t(row_index)
     stream = torch.cuda.Stream(dev)
     n_rows_scored = wl.N
-    if args.dedup:
+    if dedup:
         # candidate-preserving readout: score each distinct hidden row once
         Hu_buf = [torch.empty_like(x["H"]) for x in ins]
         with torch.cuda.stream(stream):
@@ -352,7 +357,7 @@ def measure_workload(name, args, dev, world, peaks, K, W, keep=False):
     # as a C caller holding these buffers makes it (the Python wrapper's
     # per-call checks cost more host time than a restricted pass's GPU time)
     bound = []
-    if not (args.dedup or args.gather_rows):
+    if not (dedup or args.gather_rows):
         with torch.cuda.stream(stream):
             bound = [sc.bind_call(x["H"], Wd, x["tok_row"], x["tok_ids"], x["cand_offsets"], x["set_offsets"],
                                   x["kind"], x["T"], x["mode"], x["union_ids"], out=o)[0] for x, o in zip(ins, outs)]
@@ -364,7 +369,7 @@ def measure_workload(name, args, dev, world, peaks, K, W, keep=False):
             return
         for i, (x, o) in enumerate(zip(ins, outs)):
             H, tok_row = x["H"], x["tok_row"]
-            if args.dedup:
+            if dedup:
                 H, tok_row, _ = sc.dedup_rows(H, tok_row, H_unique=Hu_buf[i])
             if args.gather_rows:
                 sc.score_sets_gather(x["H_src"], x["row_index"], Wd, tok_row, x["tok_ids"], x["cand_offsets"],
@@ -440,7 +445,7 @@ def measure_workload(name, args, dev, world, peaks, K, W, keep=False):
     t_roof = max(t_tc_burst, t_hbm)
     note = "of measured" if peaks["source"] == "measured" else "of fallback"
     rec = {
-        "name": name, "wl": wl, "steps_wl": steps_wl, "K": K, "W": W, "ms": ms, "ms_step": ms_step,
+        "name": name, "wl": wl, "steps_wl": steps_wl, "K": K, "W": W, "ms": ms, "ms_step": ms_step, "dedup": dedup,
         "value": job_throughput(tokens_per_step, K, world, ms), "tokens_per_step": tokens_per_step,
         "n_rows_scored": n_rows_scored, "plan": sc.plan_info(n_rows_scored), "clocks": clk,
         "gpu_launches": int(launches), "ms_prof": ms_prof, "prof": prof, "head_ms": head_ms,
@@ -452,7 +457,7 @@ def measure_workload(name, args, dev, world, peaks, K, W, keep=False):
                      "frac_vs_hbm": t_hbm / (head_ms / 1e3),
                      # the committed capture is of the default launch (all rows, row-major
                      # problem rows, tiled W); other configurations report none
-                     "traffic": committed_traffic(name.split("-")[0]) if not (args.dedup or args.gather_rows
+                     "traffic": committed_traffic(name.split("-")[0]) if not (dedup or args.gather_rows
                                                                              or args.w_layout != "tiled") else None,
                      "kernel": "head_lse_gather (tcgen05)", "kernel_ms": head_ms,
                      "achieved_tflops": tflops, "achieved_gbs": gbs,
@@ -513,7 +518,7 @@ def config_block(rec, args):
     return {"workload": WORKLOADS[rec["name"]][3], "d": wl.d, "V": wl.V, "N": wl.N, "n_tok": wl.n_tok,
             "n_cand": wl.n_cand, "n_sets": wl.n_sets, "modes": list(WORKLOADS[rec["name"]][1]),
             "rows_scored": rec["n_rows_scored"], "plan": rec["plan"],
-            "row_dedup": bool(args.dedup),
+            "row_dedup": bool(rec.get("dedup")),
             "weights_layout": ("tiled (jet_tile_weights once, before timing)" if args.w_layout == "tiled"
                                else "row-major"),
             "row_gather": (f"rows read in place from a right-padded [N, {args.gather_rows}, d] source "
@@ -780,7 +785,7 @@ def parse_args(argv=None):
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="large", choices=sorted(WORKLOADS),
                     help="the headline workload (default: the large 20k-row batch, the largest)")
-    ap.add_argument("--per-config", default="binary,binary-restricted,binary-both,multitoken,wideschema",
+    ap.add_argument("--per-config", default="binary,binary-restricted,binary-both,multitoken,wideschema,large-dedup",
                     help="other workloads timed the same way into the line's per_config block ('none': skip)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--w-layout", default="tiled", choices=["rowmajor", "tiled"],
