@@ -8,8 +8,9 @@ tcgen05 head, split merge, set rules.  The line's ``per_config`` block times
 the other workloads the same way: the binary batch (256 questions, d=2560,
 V=248320) in full-vocabulary mode, in restricted mode over its 26-code union
 (latency-bound: reported, not a roofline target), and both passes in one step;
-the multi-token choice batch, the wide-schema batch, and the large batch with
-each distinct hidden row projected once (the row-dedup pass inside the step).
+the binary batch with its rows read in place from a right-padded source, the
+multi-token choice batch, the wide-schema batch, and the large batch with each
+distinct hidden row projected once (the row-dedup pass inside the step).
 The metric is scored candidate tokens per second (of the first pass where a
 step holds two).
 
@@ -20,7 +21,8 @@ times come from event pairs the library records around its own launches.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
                   [--workload large|binary|multitoken|wideschema|tiny]
-                  [--per-config binary,binary-restricted,binary-both,multitoken,wideschema,large-dedup|none]
+                  [--per-config binary,binary-restricted,binary-both,binary-gather,multitoken,wideschema,
+                                large-dedup|none]
 """
 import argparse
 import hashlib
@@ -46,6 +48,10 @@ WORKLOADS = {
     "binary-restricted": ("binary_batch", ("restricted",), 6000,
                           "binary single-token batch: 256 questions x {A,B} codes, d=2560; restricted 26-code "
                           "union (T=2.179)"),
+    "binary-gather": ("binary_batch", ("full",), 6000,
+                      "binary single-token batch: 256 questions x {A,B} codes, d=2560, V=248320; full vocabulary "
+                      "(T=1); hidden rows read in place from a right-padded [256, 8, d] source "
+                      "(jet_score_sets_gather)"),
     "binary-both": ("binary_batch", ("full", "restricted"), 6000,
                     "binary single-token batch: 256 questions x {A,B} codes, d=2560, V=248320; full vocabulary "
                     "(T=1) then the restricted 26-code union (T=2.179) in one step"),
@@ -318,6 +324,7 @@ def measure_workload(name, args, dev, world, peaks, K, W, keep=False):
 
     wl, steps_wl = make_workload(name)
     dedup = bool(args.dedup) or name.endswith("-dedup")
+    gather_rows = args.gather_rows or (8 if name.endswith("-gather") else 0)
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
     Wd = t(wl.W.view(np.int16)).view(torch.bfloat16)
     ins = []
@@ -332,10 +339,10 @@ def measure_workload(name, args, dev, world, peaks, K, W, keep=False):
         Wd = sc.tile_weights(Wd)
         torch.cuda.synchronize(dev)
     outs = [sc.alloc_outputs(s.N, s.n_tok, s.n_cand, s.n_sets) for s in steps_wl]
-    if args.gather_rows:
+    if gather_rows:
         # rows read in place from a right-padded [N, L, d] source at each
         # sequence's last valid position (lengths uniform in 1..L)
-        L = args.gather_rows
+        L = gather_rows
         grng = np.random.default_rng(20261202 + 77)
         lengths = grng.integers(1, L + 1, size=wl.N)
         from workloads import to_bf16_bits as wk_to_bf16
@@ -357,7 +364,12 @@ def measure_workload(name, args, dev, world, peaks, K, W, keep=False):
     # as a C caller holding these buffers makes it (the Python wrapper's
     # per-call checks cost more host time than a restricted pass's GPU time)
     bound = []
-    if not (dedup or args.gather_rows):
+    if gather_rows and not dedup:
+        with torch.cuda.stream(stream):
+            bound = [sc.bind_gather_call(x["H_src"], x["row_index"], Wd, x["tok_row"], x["tok_ids"],
+                                         x["cand_offsets"], x["set_offsets"], x["kind"], x["T"], x["mode"],
+                                         x["union_ids"], out=o)[0] for x, o in zip(ins, outs)]
+    elif not dedup:
         with torch.cuda.stream(stream):
             bound = [sc.bind_call(x["H"], Wd, x["tok_row"], x["tok_ids"], x["cand_offsets"], x["set_offsets"],
                                   x["kind"], x["T"], x["mode"], x["union_ids"], out=o)[0] for x, o in zip(ins, outs)]
@@ -371,7 +383,7 @@ def measure_workload(name, args, dev, world, peaks, K, W, keep=False):
             H, tok_row = x["H"], x["tok_row"]
             if dedup:
                 H, tok_row, _ = sc.dedup_rows(H, tok_row, H_unique=Hu_buf[i])
-            if args.gather_rows:
+            if gather_rows:
                 sc.score_sets_gather(x["H_src"], x["row_index"], Wd, tok_row, x["tok_ids"], x["cand_offsets"],
                                      x["set_offsets"], x["kind"], x["T"], x["mode"], x["union_ids"], out=o,
                                      sync=False)
@@ -446,6 +458,7 @@ def measure_workload(name, args, dev, world, peaks, K, W, keep=False):
     note = "of measured" if peaks["source"] == "measured" else "of fallback"
     rec = {
         "name": name, "wl": wl, "steps_wl": steps_wl, "K": K, "W": W, "ms": ms, "ms_step": ms_step, "dedup": dedup,
+        "gather_rows": gather_rows,
         "value": job_throughput(tokens_per_step, K, world, ms), "tokens_per_step": tokens_per_step,
         "n_rows_scored": n_rows_scored, "plan": sc.plan_info(n_rows_scored), "clocks": clk,
         "gpu_launches": int(launches), "ms_prof": ms_prof, "prof": prof, "head_ms": head_ms,
@@ -457,7 +470,7 @@ def measure_workload(name, args, dev, world, peaks, K, W, keep=False):
                      "frac_vs_hbm": t_hbm / (head_ms / 1e3),
                      # the committed capture is of the default launch (all rows, row-major
                      # problem rows, tiled W); other configurations report none
-                     "traffic": committed_traffic(name.split("-")[0]) if not (dedup or args.gather_rows
+                     "traffic": committed_traffic(name.split("-")[0]) if not (dedup or gather_rows
                                                                              or args.w_layout != "tiled") else None,
                      "kernel": "head_lse_gather (tcgen05)", "kernel_ms": head_ms,
                      "achieved_tflops": tflops, "achieved_gbs": gbs,
@@ -521,8 +534,8 @@ def config_block(rec, args):
             "row_dedup": bool(rec.get("dedup")),
             "weights_layout": ("tiled (jet_tile_weights once, before timing)" if args.w_layout == "tiled"
                                else "row-major"),
-            "row_gather": (f"rows read in place from a right-padded [N, {args.gather_rows}, d] source "
-                           "(TMA gathers)") if args.gather_rows else None,
+            "row_gather": (f"rows read in place from a right-padded [N, {rec['gather_rows']}, d] source "
+                           "(one compaction launch, then the head's tiled loads)") if rec.get("gather_rows") else None,
             "l2": "inputs larger than L2 (W = %.2f GB > 129 MB L2)" % (wl.W.nbytes / 1e9),
             "step_roofline_us": rec["step_roofline_us"], "step_roofline_frac": rec["step_roofline_frac"],
             "kernel_ms_per_step": {k: v["ms"] / rec["K"] for k, v in rec["prof"].items() if isinstance(v, dict)},
@@ -785,7 +798,8 @@ def parse_args(argv=None):
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="large", choices=sorted(WORKLOADS),
                     help="the headline workload (default: the large 20k-row batch, the largest)")
-    ap.add_argument("--per-config", default="binary,binary-restricted,binary-both,multitoken,wideschema,large-dedup",
+    ap.add_argument("--per-config",
+                    default="binary,binary-restricted,binary-both,binary-gather,multitoken,wideschema,large-dedup",
                     help="other workloads timed the same way into the line's per_config block ('none': skip)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--w-layout", default="tiled", choices=["rowmajor", "tiled"],

@@ -383,6 +383,39 @@ class JetScorer:
 
         return call, out
 
+    def bind_gather_call(self, H_src, row_index, W, tok_row, tok_ids, cand_offsets, set_offsets, kind, T: float,
+                         mode: int = JET_MODE_FULL, union_ids=None, out: Optional[Dict[str, torch.Tensor]] = None):
+        """score_sets_gather marshalled once: returns (call, out), where call()
+        makes only the jet_score_sets_gather_async C call on the stream current
+        at bind time (the same contract as bind_call)."""
+        dev = self.device
+        _check_dev(H_src, "H_src", dev, _BF16); _check_dev(W, "W", dev, _BF16)
+        for name, t in (("row_index", row_index), ("tok_row", tok_row), ("tok_ids", tok_ids),
+                        ("cand_offsets", cand_offsets), ("set_offsets", set_offsets)):
+            _check_dev(t, name, dev, (torch.int32,))
+        _check_dev(kind, "kind", dev, (torch.uint8,))
+        if union_ids is not None:
+            _check_dev(union_ids, "union_ids", dev, (torch.int32,))
+        n_rows = row_index.numel()
+        if out is None:
+            out = self.alloc_outputs(n_rows, tok_ids.numel(), cand_offsets.numel() - 1, set_offsets.numel() - 1)
+        so = _SetOut(*[_ptr(out.get(n)) for n in SET_OUTPUTS])
+        n_union = 0 if union_ids is None else union_ids.numel()
+        args = (self._h, _ptr(H_src), H_src.shape[0], _ptr(row_index), n_rows, _ptr(W), _ptr(tok_row),
+                _ptr(tok_ids), tok_ids.numel(), _ptr(cand_offsets), cand_offsets.numel() - 1, _ptr(set_offsets),
+                _ptr(kind), set_offsets.numel() - 1, C.c_float(T), int(mode), _ptr(union_ids), n_union,
+                C.byref(so), _stream(dev))
+        fn = self.lib.jet_score_sets_gather_async
+        held = (H_src, row_index, W, tok_row, tok_ids, cand_offsets, set_offsets, kind, union_ids, out, so)
+
+        def call():
+            rc = fn(*args)
+            if rc != JET_OK:
+                raise JetError(rc, "jet_score_sets_gather")
+            return held
+
+        return call, out
+
     def bind_host_call(self, H, W, tok_row, tok_ids, cand_offsets, set_offsets, kind, T: float,
                        mode: int = JET_MODE_FULL, union_ids=None,
                        out: Optional[Dict[str, torch.Tensor]] = None, pipelined: bool = False):

@@ -1,7 +1,9 @@
-"""jet_score_sets_gather: hidden rows read in place from a larger source array
-(the answer positions of a right-padded backbone output), through the head's
-TMA row gathers.  The gathered call must reproduce the compact call on the same
-rows bit for bit (same bytes reach the same arithmetic), and match the oracle."""
+"""jet_score_sets_gather: hidden rows read from a larger source array (the
+answer positions of a right-padded backbone output): copied once into the
+context's staging rows for the tcgen05 head, or read in place by the small
+restricted kernel.  The gathered call must reproduce the compact call on the
+same rows bit for bit (same bytes reach the same arithmetic), and match the
+oracle."""
 import numpy as np
 import pytest
 import torch
@@ -113,3 +115,18 @@ def test_gather_rejects_bad_indices(jet):
         out = sc.score_sets_gather(S, dev(row_index), W, *args)      # the context still works
         torch.cuda.synchronize()
         compare(w, {k: v.cpu().numpy() for k, v in out.items()}, oracle.score_workload(w))
+
+
+def test_bound_gather_call_matches_gather(jet):
+    """bind_gather_call marshals once; each call() is the bare asynchronous
+    gather call, bit-identical to score_sets_gather."""
+    wl = wk.binary_batch(n_questions=200, random_pairs=True, d=128, V=1500)
+    src, row_index = padded_source(wl, 5, L=8)
+    sc = jet.JetScorer(wl.d, wl.V, wl.N, wl.n_tok)
+    args = (dev(src.view(np.int16)).view(torch.bfloat16), dev(row_index), dev(wl.W.view(np.int16)).view(torch.bfloat16),
+            dev(wl.tok_row), dev(wl.tok_ids), dev(wl.cand_offsets), dev(wl.set_offsets), dev(wl.kind), wl.T)
+    ref = sc.score_sets_gather(*args)
+    call, out = sc.bind_gather_call(*args)
+    call()
+    assert sc.sync_status() == 0
+    assert_bitwise({k: v.cpu().numpy() for k, v in out.items()}, {k: v.cpu().numpy() for k, v in ref.items()})
