@@ -11,8 +11,10 @@ V=248320) in full-vocabulary mode, in restricted mode over its 26-code union
 the binary batch with its rows read in place from a right-padded source, the
 multi-token choice batch, the wide-schema batch, and the large batch with each
 distinct hidden row projected once (the row-dedup pass inside the step).
-The metric is scored candidate tokens per second (of the first pass where a
-step holds two).
+The ``ops`` block times the widened ops at the same steps: row dedup of the
+large batch's rows, temperature fitting, layer sensitivity, and restricted
+mode over unions of 600 and 4096 codes.  The metric is scored candidate
+tokens per second (of the first pass where a step holds two).
 
 Printed: one JSON line (rank 0).  Timing: CUDA events on the launching stream,
 after warm-up, synchronised on both sides; W (0.8-1.3 GB) is larger than L2, so
@@ -636,6 +638,14 @@ def gpu_arm(args, world, rank, local):
                         "clocks": r["clocks"]})
             line["per_config"][other] = blk
 
+    # the widened ops and restricted mode over larger unions, at the same steps
+    if world == 1 and args.ops not in ("", "none"):
+        line["ops"] = {}
+        for op in args.ops.split(","):
+            rec = run_op(op, args, K, W, "600,4096")
+            rec.pop("op", None)
+            line["ops"][op] = rec
+
     # CPU oracle baseline on a bounded sample (rank 0, one GPU only)
     if world == 1 and not args.no_cpu_baseline:
         import oracle
@@ -675,21 +685,29 @@ def time_op(fn, K, W):
 
 def op_arm(args):
     """One JSON line for a widened op (not the headline scoring metric)."""
+    from candidate_answer_scoring_gb300 import build as libbuild
+    libbuild.build()
+    K = args.steps if args.steps is not None else 50
+    W = max(3, args.warmup if args.warmup is not None else 5)
+    line = run_op(args.op, args, K, W, args.unions)
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_op(op, args, K, W, unions):
+    """Time one widened op (row dedup, temperature fit, layer sensitivity) or
+    restricted mode over the given union sizes; returns its record."""
     import numpy as np
     import torch
 
     import candidate_answer_scoring_gb300 as jet
     import workloads as wk
-    from candidate_answer_scoring_gb300 import build as libbuild
-    libbuild.build()
     peaks = load_peaks()
     dev = torch.device("cuda", 0)
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
-    K = args.steps if args.steps is not None else 50
-    W = max(3, args.warmup if args.warmup is not None else 5)
-    line = {"op": args.op, "n_gpus": 1, "steps": K, "warmup": W, "data": "synthetic"}
-    if args.op == "dedup":
-        wl = wk.large_choice()
+    line = {"op": op, "n_gpus": 1, "steps": K, "warmup": W, "data": "synthetic"}
+    if op == "dedup":
+        wl = make_workload("large")[0]
         sc = jet.JetScorer(wl.d, wl.V, wl.N, wl.n_tok)
         H = t(wl.H.view(np.int16)).view(torch.bfloat16)
         tok_row = t(wl.tok_row)
@@ -702,11 +720,11 @@ def op_arm(args):
                     roofline={"bound": "hbm", "achieved": nbytes / (ms / 1e3) / 1e9, "peak": peaks["hbm"],
                               "unit": "GB/s", "frac": nbytes / (ms / 1e3) / 1e9 / peaks["hbm"],
                               "note": "synchronous call: includes the count read-back"})
-    elif args.op == "fit_temperature":
+    elif op == "fit_temperature":
         # scores s(c) of the wide-schema batch from the library's own scoring
         # call; gold labels drawn from q = softmax(s / T0) with T0 = 2.179, so
         # the fit has an interior optimum near T0
-        wl = wk.wide_schema()
+        wl = make_workload("wideschema")[0]
         scorer = jet.JetScorer(wl.d, wl.V, wl.N, wl.n_tok)
         Wd = t(wl.W.view(np.int16)).view(torch.bfloat16)
         out = scorer.score_sets(t(wl.H.view(np.int16)).view(torch.bfloat16), Wd, t(wl.tok_row), t(wl.tok_ids),
@@ -730,13 +748,13 @@ def op_arm(args):
                     config={"workload": "wide schema: %d sets, %d candidates; gold drawn from q at T0 = %.3f"
                                         % (wl.n_sets, wl.n_cand, T0)},
                     roofline={"bound": "latency", "note": "one CTA, bracketed Newton on 1/T; synchronous call"})
-    elif args.op == "restricted":
+    elif op == "restricted":
         # restricted mode on the binary batch's shape (256 questions, one row
         # each, d=2560, V=248320) over unions of several sizes: each question a
         # binary pair of codes drawn from the union
         line.update(metric="restricted-mode candidate tokens scored per second", unit="tokens/s", per_union={})
         W_dev = None
-        for n_union in [int(x) for x in args.unions.split(",")]:
+        for n_union in [int(x) for x in unions.split(",")]:
             wl = wk.union_choice(256, n_union)
             if W_dev is None:
                 W_dev = t(wl.W.view(np.int16)).view(torch.bfloat16)
@@ -771,7 +789,7 @@ def op_arm(args):
         line["config"] = {"workload": "256 questions x binary pair of codes from the union, d=2560, V=248320, "
                                       "one row per question, T=2.179; asynchronous calls back to back",
                           "weights_layout": args.w_layout, "peaks": peaks["source"]}
-    elif args.op == "layer_sensitivity":
+    elif op == "layer_sensitivity":
         rng = np.random.default_rng(0)
         n, L, m = 4096, 64, 64
         offsets = np.arange(0, n * m + 1, m, dtype=np.int32)
@@ -786,8 +804,9 @@ def op_arm(args):
                     roofline={"bound": "hbm", "achieved": nbytes / (ms / 1e3) / 1e9, "peak": peaks["hbm"],
                               "unit": "GB/s", "frac": nbytes / (ms / 1e3) / 1e9 / peaks["hbm"],
                               "note": "synchronous call: includes the status read-back"})
-    print(json.dumps(line), flush=True)
-    return 0
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return line
 
 
 def parse_args(argv=None):
@@ -813,6 +832,8 @@ def parse_args(argv=None):
                     help="time one of the widened ops, or restricted mode over larger unions, instead of the "
                          "scoring path")
     ap.add_argument("--unions", default="26,256,600,4096", help="union sizes for --op restricted")
+    ap.add_argument("--ops", default="dedup,fit_temperature,layer_sensitivity,restricted",
+                    help="widened ops timed into the line's ops block ('none': skip; restricted: 600 and 4096 codes)")
     return ap.parse_args(argv)
 
 
