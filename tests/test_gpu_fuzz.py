@@ -2,7 +2,8 @@
 sizes (ragged against the 256-column tiles), set counts and sizes, candidate
 lengths, kinds, duplicate rates, temperatures and row layouts in full mode;
 unions of 1 to 150 codes (one to five 32-code groups of the restricted head)
-in restricted mode.  Every case is fixed by its seed, so a failure reproduces."""
+and of 192 to 4096 codes (the tcgen05 head over the staged union) in
+restricted mode.  Every case is fixed by its seed, so a failure reproduces."""
 import numpy as np
 import pytest
 
@@ -56,6 +57,36 @@ def restricted_case(seed):
     W = wk.gen_W(7000 + seed, V, d)
     wl = wk._build(f"fuzz-restricted-{seed}", 7000 + seed, d, V, W, sets, T, row_mode="per_key")
     return wl.with_mode(wk.MODE_RESTRICTED, T, union)
+
+
+def restricted_union_case(seed):
+    """Unions the tcgen05 head serves: 192 to 4096 codes (ragged against the
+    256-column tiles), sets of up to 40 codes with duplicates, rows shared by
+    a set's codes."""
+    rng = np.random.default_rng(3000 + seed)
+    d = int(rng.choice(D_CHOICES))
+    n_union = int(rng.integers(192, 4097))
+    V = int(rng.integers(n_union + 1, n_union + 6000))
+    union = rng.choice(V, size=n_union, replace=False).astype(np.int32)
+    sets = []
+    for _ in range(int(rng.integers(1, 120))):
+        K = int(rng.integers(1, 41))
+        codes = rng.choice(union, size=K, replace=False)
+        if K > 1 and rng.random() < 0.3:
+            codes[-1] = codes[0]                    # a duplicated code within the set
+        sets.append(wk._SetSpec(wk.KIND_CHOICE, [(int(t),) for t in codes]))
+    T = float(rng.choice(T_CHOICES))
+    W = wk.gen_W(8000 + seed, V, d)
+    wl = wk._build(f"fuzz-union-{seed}", 8000 + seed, d, V, W, sets, T, row_mode="per_key")
+    return wl.with_mode(wk.MODE_RESTRICTED, T, union)
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_fuzz_restricted_large_union(jet, seed):
+    wl = restricted_union_case(seed)
+    gpu = run_gpu(jet, wl)
+    compare(wl, gpu, oracle.score_workload(wl))
+    check_duplicates(wl, gpu)
 
 
 @pytest.mark.parametrize("seed", range(40))
