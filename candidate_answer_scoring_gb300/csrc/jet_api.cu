@@ -442,6 +442,34 @@ int score_sets_enqueue(jet_ctx* c, const void* H, const void* W, int n_rows, con
   return cuda_status(launch_sets(sa, st));
 }
 
+// Host-buffer entries: the caller's requested outputs (*out_host, host
+// pointers; NULL members not wanted) get device places behind the error words
+// in the context's output block, 16-byte aligned; *h receives the host
+// pointers, *dev the device ones.  Returns the bytes of the block in use.
+size_t place_host_outputs(jet_ctx* c, const jet_set_out* out_host, int n_rows, int n_tok, int n_cand, int n_sets,
+                          jet_set_out* h, jet_set_out* dev) {
+  std::memset(h, 0, sizeof *h);
+  if (out_host) *h = *out_host;
+  std::memset(dev, 0, sizeof *dev);
+  size_t off = IO_HEAD;
+  auto place = [&](void* host_ptr, size_t bytes) -> uint8_t* {
+    if (!host_ptr) return nullptr;
+    uint8_t* p = c->io_dev + off;
+    off += (bytes + 15) & ~size_t(15);
+    return p;
+  };
+  dev->logp = reinterpret_cast<float*>(place(h->logp, (size_t)n_tok * 4));
+  dev->lse = reinterpret_cast<float*>(place(h->lse, (size_t)n_rows * 4));
+  dev->s = reinterpret_cast<float*>(place(h->s, (size_t)n_cand * 4));
+  dev->q = reinterpret_cast<float*>(place(h->q, (size_t)n_cand * 4));
+  dev->q_equiv = reinterpret_cast<float*>(place(h->q_equiv, (size_t)n_cand * 4));
+  dev->decision = reinterpret_cast<int32_t*>(place(h->decision, (size_t)n_sets * 4));
+  dev->expected = reinterpret_cast<float*>(place(h->expected, (size_t)n_sets * 4));
+  dev->confidence = reinterpret_cast<float*>(place(h->confidence, (size_t)n_sets * 4));
+  dev->mass = reinterpret_cast<float*>(place(h->mass, (size_t)n_sets * 4));
+  return off;
+}
+
 int read_status(jet_ctx* c, cudaStream_t st) {
   if (cudaMemcpyAsync(c->h_err, c->err, ERR_WORDS * sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess)
     return JET_ERR_CUDA;
@@ -895,27 +923,8 @@ int jet_score_sets_host(jet_ctx* c, const void* H, const void* W, int n_rows, co
     return JET_ERR_CUDA;
 
   // outputs: the requested ones behind the error words, in one device block
-  jet_set_out h;
-  std::memset(&h, 0, sizeof h);
-  if (out_host) h = *out_host;
-  jet_set_out dev;
-  std::memset(&dev, 0, sizeof dev);
-  size_t out_off = IO_HEAD;
-  auto place = [&](void* host_ptr, size_t bytes) -> uint8_t* {
-    if (!host_ptr) return nullptr;
-    uint8_t* p = c->io_dev + out_off;
-    out_off += (bytes + 15) & ~size_t(15);
-    return p;
-  };
-  dev.logp = reinterpret_cast<float*>(place(h.logp, (size_t)n_tok * 4));
-  dev.lse = reinterpret_cast<float*>(place(h.lse, (size_t)n_rows * 4));
-  dev.s = reinterpret_cast<float*>(place(h.s, (size_t)n_cand * 4));
-  dev.q = reinterpret_cast<float*>(place(h.q, (size_t)n_cand * 4));
-  dev.q_equiv = reinterpret_cast<float*>(place(h.q_equiv, (size_t)n_cand * 4));
-  dev.decision = reinterpret_cast<int32_t*>(place(h.decision, (size_t)n_sets * 4));
-  dev.expected = reinterpret_cast<float*>(place(h.expected, (size_t)n_sets * 4));
-  dev.confidence = reinterpret_cast<float*>(place(h.confidence, (size_t)n_sets * 4));
-  dev.mass = reinterpret_cast<float*>(place(h.mass, (size_t)n_sets * 4));
+  jet_set_out h, dev;
+  const size_t out_off = place_host_outputs(c, out_host, n_rows, n_tok, n_cand, n_sets, &h, &dev);
   rc = score_sets_enqueue(c, c->stH, W, n_rows, d_row, d_tok, n_tok, d_co, n_cand, d_so, d_kind, n_sets, T, mode,
                           d_union, n_union, &dev, st);
   if (rc != JET_OK) {
@@ -1021,27 +1030,8 @@ int jet_score_sets_host_async(jet_ctx* c, const void* H, const void* W, int n_ro
 
   // outputs: written by the kernels into the output block (in stream order,
   // so the next call's kernels come after these copies), copied to the caller
-  jet_set_out h;
-  std::memset(&h, 0, sizeof h);
-  if (out_host) h = *out_host;
-  jet_set_out dev;
-  std::memset(&dev, 0, sizeof dev);
-  size_t out_off = IO_HEAD;
-  auto place = [&](void* host_ptr, size_t bytes) -> uint8_t* {
-    if (!host_ptr) return nullptr;
-    uint8_t* p = c->io_dev + out_off;
-    out_off += (bytes + 15) & ~size_t(15);
-    return p;
-  };
-  dev.logp = reinterpret_cast<float*>(place(h.logp, (size_t)n_tok * 4));
-  dev.lse = reinterpret_cast<float*>(place(h.lse, (size_t)n_rows * 4));
-  dev.s = reinterpret_cast<float*>(place(h.s, (size_t)n_cand * 4));
-  dev.q = reinterpret_cast<float*>(place(h.q, (size_t)n_cand * 4));
-  dev.q_equiv = reinterpret_cast<float*>(place(h.q_equiv, (size_t)n_cand * 4));
-  dev.decision = reinterpret_cast<int32_t*>(place(h.decision, (size_t)n_sets * 4));
-  dev.expected = reinterpret_cast<float*>(place(h.expected, (size_t)n_sets * 4));
-  dev.confidence = reinterpret_cast<float*>(place(h.confidence, (size_t)n_sets * 4));
-  dev.mass = reinterpret_cast<float*>(place(h.mass, (size_t)n_sets * 4));
+  jet_set_out h, dev;
+  place_host_outputs(c, out_host, n_rows, n_tok, n_cand, n_sets, &h, &dev);
   rc = score_sets_enqueue(c, stH, W, n_rows, d_row, d_tok, n_tok, d_co, n_cand, d_so, d_kind, n_sets, T, mode,
                           d_union, n_union, &dev, st);
   if (rc != JET_OK) {
