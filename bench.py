@@ -544,6 +544,47 @@ def config_block(rec, args):
             "ms_per_step_with_kernel_events": rec["ms_prof"] / rec["K"]}
 
 
+def _round(x, sig=5):
+    """Floats to sig significant digits (the line stays short enough for a
+    bounded log tail); everything else unchanged, recursively."""
+    if isinstance(x, float):
+        return float(f"{x:.{sig}g}")
+    if isinstance(x, dict):
+        return {k: _round(v, sig) for k, v in x.items()}
+    if isinstance(x, list):
+        return [_round(v, sig) for v in x]
+    return x
+
+
+def compact_config(rec, K, W):
+    """One per_config entry: the workload's sizes, throughput, step and head
+    time, the roofline of its dominant kernel and the clocks seen."""
+    wl, rf = rec["wl"], rec["roofline"]
+    keep = ("bound", "achieved", "peak", "unit", "frac", "frac_vs_burst_tensor", "frac_vs_sustained_tensor",
+            "traffic", "kernel_ms", "n_union")
+    clk = rec["clocks"] or {}
+    out = {"d": wl.d, "V": wl.V, "N": wl.N, "n_tok": wl.n_tok, "rows_scored": rec["n_rows_scored"],
+           "value": rec["value"], "unit": UNIT, "steps": K, "warmup": W, "ms_per_step": rec["ms_step"],
+           "head_ms": rec["head_ms"], "step_roofline_frac": rec["step_roofline_frac"],
+           "gpu_launches": rec["gpu_launches"],
+           "roofline": {k: rf[k] for k in keep if k in rf},
+           "clocks": {k: clk.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons")}}
+    return _round(out)
+
+
+def compact_op(rec):
+    """One ops entry: its rate, time per call and roofline note."""
+    out = {k: rec[k] for k in ("metric", "value", "unit", "ms", "T") if k in rec}
+    if "roofline" in rec:
+        out["roofline"] = {k: rec["roofline"][k] for k in ("bound", "achieved", "unit", "frac", "note")
+                           if k in rec["roofline"]}
+    if "per_union" in rec:
+        out["per_union"] = {u: {"path": v["path"], "us_per_call": v["us_per_call"],
+                                "projection_us": v["projection_us"], "roofline_us": v["roofline_us"]}
+                            for u, v in rec["per_union"].items()}
+    return _round(out)
+
+
 def gpu_arm(args, world, rank, local):
     import numpy as np
     import torch
@@ -632,19 +673,13 @@ def gpu_arm(args, world, rank, local):
         line["per_config"] = {}
         for other in others:
             r = measure_workload(other, args, dev, world, peaks, K, W)
-            blk = config_block(r, args)
-            blk.update({"value": r["value"], "unit": UNIT, "steps": K, "warmup": W, "ms_per_step": r["ms_step"],
-                        "head_ms": r["head_ms"], "gpu_launches": r["gpu_launches"], "roofline": r["roofline"],
-                        "clocks": r["clocks"]})
-            line["per_config"][other] = blk
+            line["per_config"][other] = compact_config(r, K, W)
 
     # the widened ops and restricted mode over larger unions, at the same steps
     if world == 1 and args.ops not in ("", "none"):
         line["ops"] = {}
         for op in args.ops.split(","):
-            rec = run_op(op, args, K, W, "600,4096")
-            rec.pop("op", None)
-            line["ops"][op] = rec
+            line["ops"][op] = compact_op(run_op(op, args, K, W, "600,4096"))
 
     # CPU oracle baseline on a bounded sample (rank 0, one GPU only)
     if world == 1 and not args.no_cpu_baseline:
@@ -658,8 +693,9 @@ def gpu_arm(args, world, rank, local):
             "sample": f"first {n_cand} of {wl.n_cand} candidates ({ntok} full-vocab tokens over {sub.N} hidden "
                       f"rows{', plus the restricted pass' if len(steps_wl) > 1 else ''}); {dt:.1f} s",
         }
+    line["per_config_workloads"] = {w: WORKLOADS[w][3] for w in line.get("per_config", {})}
     if rank == 0:
-        print(json.dumps(line), flush=True)
+        print(json.dumps(_round(line, 7)), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
     return 0
