@@ -106,14 +106,18 @@ def committed_traffic(workload):
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    """nvidia-smi samples of SM clock and throttle reasons, every 200 ms; the
+    statistics cover the samples received during the marked timed passes (or,
+    for a pass shorter than the sampling period, the first sample after its
+    start)."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_id):
-        self.rows = []
+        self.rows = []        # (host receive time, fields)
+        self.windows = []     # (start, end) host times of the timed passes
         self.proc = None
         self.gpu_id = gpu_id
 
@@ -133,7 +137,10 @@ class ClockSampler:
         for line in self.proc.stdout:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) >= 8:
-                self.rows.append(parts)
+                self.rows.append((time.monotonic(), parts))
+
+    def mark(self, t0, t1):
+        self.windows.append((t0, t1))
 
     def stop(self):
         if self.proc is None:
@@ -145,14 +152,24 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.thread.join(timeout=2)
-        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
-        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        return self.summary()
+
+    def summary(self):
+        picked = []
+        for t0, t1 in self.windows:
+            inside = [r for t, r in self.rows if t0 <= t <= t1]
+            after = [r for t, r in self.rows if t > t0][:1]
+            picked += inside if inside else after
+        rows = picked if picked else [r for _, r in self.rows]
+        num = lambda v: v.replace(".", "").isdigit()
+        sm = [float(r[0]) for r in rows if num(r[0])]
+        mx = [float(r[1]) for r in rows if num(r[1])]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({n for r in self.rows for n, v in zip(names, r[4:8]) if v.lower() == "active"})
-        pw = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[4:8]) if v.lower() == "active"})
+        pw = [float(r[2]) for r in rows if num(r[2])]
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(self.rows),
-                "power_w_max": max(pw) if pw else None}
+                "reasons": reasons, "samples": len(rows),
+                "window_s": sum(t1 - t0 for t0, t1 in self.windows), "power_w_max": max(pw) if pw else None}
 
 
 def dist_setup():
@@ -422,11 +439,15 @@ def measure_workload(name, args, dev, world, peaks, K, W, keep=False):
 
         # (1) the step as a user runs it: no event records between kernels,
         # so each kernel's launch overlaps the previous one's tail
+        h0 = time.monotonic()
         ms = timed(K)
+        clocks.mark(h0, time.monotonic())
         # (2) the same loop with the library's per-launch event pairs, for the
         # kernel-level roofline (events between kernels remove that overlap)
         sc.profile(True)
+        h0 = time.monotonic()
         ms_prof = timed(K)
+        clocks.mark(h0, time.monotonic())
         prof = sc.profile_read()
         sc.profile(False)
         clk = clocks.stop()

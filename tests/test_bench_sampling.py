@@ -51,3 +51,18 @@ def test_subset_of_restricted_pass_keeps_union():
     assert sub.union_ids is r.union_ids and sub.mode == r.mode
     res = oracle.score_workload(sub)
     np.testing.assert_array_equal(res.s, oracle.score_workload(r).s[:3])
+
+
+def test_clock_summary_covers_the_timed_passes():
+    """Clock statistics come from the samples received during the marked
+    passes; a pass shorter than the sampling period takes the first sample
+    after its start; idle samples outside them are not counted."""
+    idle = ["2070", "2070", "150", "0x0", "Not Active", "Not Active", "Not Active", "Not Active"]
+    busy = ["1800", "2070", "1300", "0x4", "Not Active", "Not Active", "Not Active", "Active"]
+    c = bench.ClockSampler(None)
+    c.rows = [(0.0, idle), (0.2, idle), (0.4, busy), (0.6, busy), (0.8, idle), (1.0, busy), (1.2, idle)]
+    c.mark(0.3, 0.7)          # two samples inside
+    c.mark(0.9, 0.95)         # none inside: the first after its start
+    s = c.summary()
+    assert s["samples"] == 3 and s["sm_mhz"] == 1800.0 and s["reasons"] == ["sw_power_cap"]
+    assert abs(s["window_s"] - 0.45) < 1e-9
