@@ -1,8 +1,9 @@
-// Device pre-pass of the full-vocabulary path: validates every index the rest
-// of the path will use and
-// builds, per hidden row, the list of scored tokens it predicts (sorted by
-// token id), which the head's epilogue walks while it sweeps vocabulary
-// tiles.
+// Device pre-pass of the tcgen05 path: validates every index the rest of the
+// path will use and builds, per hidden row, the list of scored tokens it
+// predicts (sorted by the column each is gathered from: its token id, or in
+// restricted mode over a staged union its union position, after the
+// restricted checks), which the head's epilogue walks while it sweeps
+// vocabulary tiles.
 // Three layouts: one token per row (jet_score_tokens), tokens already grouped
 // by row (tok_row non-decreasing: row pointers from run boundaries), and the
 // general case (count, scan, scatter).
@@ -152,7 +153,7 @@ __global__ void __launch_bounds__(PREP_THREADS) prep_kernel(PrepArgs a) {
       a.row_list[j] = make_int2(list_key(a, j), j);
     }
     __syncthreads();
-    for (int r = tid; r < a.n_rows; r += nth) {      // order each row's tokens by id
+    for (int r = tid; r < a.n_rows; r += nth) {      // order each row's tokens by column
       const int b = a.row_ptr[r], e = a.row_ptr[r + 1];
       for (int i = b + 1; i < e; ++i) {
         const int2 x = a.row_list[i];
@@ -213,7 +214,7 @@ __global__ void __launch_bounds__(PREP_THREADS) prep_kernel(PrepArgs a) {
   }
   __syncthreads();
 
-  // sort each row's list by (token id, token index): rows hold few tokens
+  // sort each row's list by (column, token index): rows hold few tokens
   for (int r = tid; r < a.n_rows; r += nth) {
     const int b = a.row_ptr[r], e = a.row_ptr[r + 1];
     for (int i = b + 1; i < e; ++i) {
