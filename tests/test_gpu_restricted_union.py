@@ -180,6 +180,13 @@ def test_union_head_status_codes(jet):
     m = args_of(multi, mode=wk.MODE_RESTRICTED, union_ids=dev(np.arange(2000, dtype=np.int32)))
     sc2 = jet.JetScorer(64, 2000, multi.N, multi.n_tok)
     assert status(jet, sc2, m) == MODE                                       # two-token candidates
+    # a union longer than the vocabulary (so it repeats ids) exceeds the staging
+    # rows and is taken by the mma.sync path, which reports the repeat
+    small = wk.union_choice(10, 200, K=(2, 3), d=64, V=250, seed_offset=5)
+    longer = np.concatenate([small.union_ids, small.union_ids[:100]]).astype(np.int32)   # 300 ids, V = 250
+    sc3 = jet.JetScorer(64, 250, small.N, small.n_tok)
+    assert status(jet, sc3, args_of(small, union_ids=dev(longer))) == UNION
+    assert status(jet, sc3, args_of(small)) == OK
     assert status(jet, sc, a) == OK
     compare(wl, run(sc, a), oracle.score_workload(wl))
 
