@@ -354,6 +354,34 @@ def test_pipelined_host_calls_match_host_entry(jet):
         assert np.array_equal(calls[3][1][k].numpy().view(np.uint32), batches[1][1][k].numpy().view(np.uint32)), k
 
 
+def test_pipelined_host_calls_past_the_status_ring(jet):
+    """More pipelined calls between two waits than the context keeps status
+    words for (4096): the call past the ring waits for the earlier ones and
+    keeps their first rejection, which the wait still returns; a clean run of
+    the same length returns JET_OK and the last call's outputs equal the
+    synchronous host entry bit for bit."""
+    a = wk.custom(64, 300, 6, K=(2, 3), length=(1, 2), seed=31)
+    sc = jet.JetScorer(a.d, a.V, a.N, a.n_tok)
+    W = to_dev(a)["W"]
+    pin = lambda x: torch.from_numpy(np.ascontiguousarray(x)).pin_memory()
+    args = (pin(a.H.view(np.int16)).view(torch.bfloat16), W, pin(a.tok_row), pin(a.tok_ids),
+            pin(a.cand_offsets), pin(a.set_offsets), pin(a.kind), a.T)
+    ref = sc.score_sets_host(*args)
+    good, out = sc.bind_host_call(*args, pipelined=True)
+    bad_ids = args[3].clone().pin_memory()
+    bad_ids[0] = a.V
+    bad, _ = sc.bind_host_call(args[0], W, args[2], bad_ids, *args[4:], pipelined=True)
+    n = 4096 + 5
+    for i in range(n):
+        (bad if i == 3 else good)()
+    assert sc.host_wait() == -2                # JET_ERR_TOKEN_RANGE, from before the ring filled
+    for _ in range(n):
+        good()
+    assert sc.host_wait() == 0
+    for k in OUT_KEYS:
+        assert np.array_equal(out[k].numpy().view(np.uint32), ref[k].numpy().view(np.uint32)), k
+
+
 def test_bound_device_call_matches_score_sets(jet):
     """bind_call marshals once; each call() is the bare asynchronous C call on
     the same device buffers: bit-identical to score_sets in full and
