@@ -195,14 +195,23 @@ def test_edge_cases(jet):
     compare(wl, gpu, oracle.score_workload(wl))
 
 
-@pytest.mark.parametrize("case", ["vocab-below-one-tile", "widest-rows", "single-code-union", "million-vocab"])
+@pytest.mark.parametrize("case", ["vocab-below-one-tile", "one-token-vocab", "widest-rows", "single-code-union",
+                                  "million-vocab"])
 def test_shape_extremes(jet, case):
-    """A vocabulary smaller than one 256-column tile (every column ragged), the
-    widest rows the library accepts (d = 16384: 256 k-blocks per tile) through
-    the full-vocabulary head with both head variants' row counts, and a
-    restricted union of one code (lse_U = z, so logp = 0 and q = 1)."""
+    """A vocabulary smaller than one 256-column tile (every column ragged), a
+    vocabulary of one token (lse = z, so every logp is 0, every candidate
+    scores 0 and each set's q is uniform), the widest rows the library accepts
+    (d = 16384: 256 k-blocks per tile) through the full-vocabulary head with
+    both head variants' row counts, and a restricted union of one code
+    (lse_U = z, so logp = 0 and q = 1)."""
     if case == "vocab-below-one-tile":
         wls = [wk.custom(64, 100, 6, K=(1, 5), length=(1, 3), seed=91)]
+    elif case == "one-token-vocab":
+        sets = [wk._SetSpec(wk.KIND_CHOICE, [(0,), (0, 0), (0, 0, 0)]), wk._SetSpec(wk.KIND_BINARY, [(0,), (0,)]),
+                wk._SetSpec(wk.KIND_ORDINAL, [(0,)] * 5), wk._SetSpec(wk.KIND_CHOICE, [(0,)])]
+        wls = [wk._build("one-token-vocab", 55, 64, 1, wk.gen_W(55, 1, 64), sets, 1.0, row_mode="per_token")]
+        single = wk._build("one-token-vocab-single", 56, 64, 1, wk.gen_W(56, 1, 64), sets[1:], 1.0)
+        wls += [single, single.with_mode(wk.MODE_RESTRICTED, 2.0, np.zeros(1, dtype=np.int32))]
     elif case == "widest-rows":
         wls = [wk.custom(16384, 700, 4, K=(2, 4), length=(1, 2), seed=92),      # N <= 128: one-CTA head
                wk.binary_batch(150, random_pairs=True, d=16384, V=600)]          # N > 128: paired head
@@ -222,6 +231,9 @@ def test_shape_extremes(jet, case):
         compare(wl, gpu, oracle.score_workload(wl))
         if case == "single-code-union":
             assert np.all(gpu["logp"] == 0.0) and np.all(gpu["q"] == 1.0)
+        if case == "one-token-vocab":
+            assert np.abs(gpu["logp"]).max() <= 1e-6
+            np.testing.assert_array_equal(gpu["decision"], 0)       # all tied: the first candidate
 
 
 @pytest.mark.parametrize("T", [0.02, 0.25, 50.0])
