@@ -9,8 +9,10 @@ the other workloads the same way: the binary batch (256 questions, d=2560,
 V=248320) in full-vocabulary mode, in restricted mode over its 26-code union
 (latency-bound: reported, not a roofline target), and both passes in one step;
 the binary batch with its rows read in place from a right-padded source, the
-multi-token choice batch, the wide-schema batch, and the large batch with each
-distinct hidden row projected once (the row-dedup pass inside the step).
+multi-token choice batch, the wide-schema batch, the large batch with each
+distinct hidden row projected once (the row-dedup pass inside the step), and
+the large batch with W in the library's default row-major layout (every other
+entry streams W packed once by jet_tile_weights).
 The ``ops`` block times the widened ops at the same steps: row dedup of the
 large batch's rows, temperature fitting, layer sensitivity, and restricted
 mode over unions of 600 and 4096 codes.  The metric is scored candidate
@@ -24,7 +26,7 @@ times come from event pairs the library records around its own launches.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
                   [--workload large|binary|multitoken|wideschema|tiny]
                   [--per-config binary,binary-restricted,binary-both,binary-gather,multitoken,wideschema,
-                                large-dedup|none]
+                                large-dedup,large-rowmajor|none]
 """
 import argparse
 import hashlib
@@ -66,6 +68,9 @@ WORKLOADS = {
     "large-dedup": ("large_choice", ("full",), 40,
                     "large choice: 16 requests x K=64, 8-32 tokens, d=4096, V=152064, T=1; each distinct hidden "
                     "row projected once (jet_dedup_rows inside the step)"),
+    "large-rowmajor": ("large_choice", ("full",), 40,
+                       "large choice: 16 requests x K=64, 8-32 tokens, d=4096, V=152064, T=1; W read in the "
+                       "library's default row-major [V, d] layout (no jet_tile_weights)"),
     "tiny": ("tiny", ("full",), 2000, "tiny: d=64, V=1000, 3 sets"),
 }
 
@@ -344,6 +349,7 @@ def measure_workload(name, args, dev, world, peaks, K, W, keep=False):
     wl, steps_wl = make_workload(name)
     dedup = bool(args.dedup) or name.endswith("-dedup")
     gather_rows = args.gather_rows or (8 if name.endswith("-gather") else 0)
+    w_layout = "rowmajor" if name.endswith("-rowmajor") else args.w_layout
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
     Wd = t(wl.W.view(np.int16)).view(torch.bfloat16)
     ins = []
@@ -352,7 +358,7 @@ def measure_workload(name, args, dev, world, peaks, K, W, keep=False):
                         cand_offsets=t(s.cand_offsets), set_offsets=t(s.set_offsets), kind=t(s.kind),
                         union_ids=None if s.union_ids is None else t(s.union_ids), T=s.T, mode=s.mode, wl=s))
     sc = jet.JetScorer(wl.d, wl.V, wl.N, wl.n_tok, device=dev.index)
-    if args.w_layout == "tiled":
+    if w_layout == "tiled":
         # the output embedding is stored once in the head's tiled layout (as a
         # model loader would), outside the timed region
         Wd = sc.tile_weights(Wd)
@@ -481,7 +487,7 @@ def measure_workload(name, args, dev, world, peaks, K, W, keep=False):
     note = "of measured" if peaks["source"] == "measured" else "of fallback"
     rec = {
         "name": name, "wl": wl, "steps_wl": steps_wl, "K": K, "W": W, "ms": ms, "ms_step": ms_step, "dedup": dedup,
-        "gather_rows": gather_rows,
+        "gather_rows": gather_rows, "w_layout": w_layout,
         "value": job_throughput(tokens_per_step, K, world, ms), "tokens_per_step": tokens_per_step,
         "n_rows_scored": n_rows_scored, "plan": sc.plan_info(n_rows_scored), "clocks": clk,
         "gpu_launches": int(launches), "ms_prof": ms_prof, "prof": prof, "head_ms": head_ms,
@@ -494,7 +500,7 @@ def measure_workload(name, args, dev, world, peaks, K, W, keep=False):
                      # the committed capture is of the default launch (all rows, row-major
                      # problem rows, tiled W); other configurations report none
                      "traffic": committed_traffic(name.split("-")[0]) if not (dedup or gather_rows
-                                                                             or args.w_layout != "tiled") else None,
+                                                                             or w_layout != "tiled") else None,
                      "kernel": "head_lse_gather (tcgen05)", "kernel_ms": head_ms,
                      "achieved_tflops": tflops, "achieved_gbs": gbs,
                      "algorithmic_bytes": bytes_, "algorithmic_flops": flops,
@@ -555,7 +561,7 @@ def config_block(rec, args):
             "n_cand": wl.n_cand, "n_sets": wl.n_sets, "modes": list(WORKLOADS[rec["name"]][1]),
             "rows_scored": rec["n_rows_scored"], "plan": rec["plan"],
             "row_dedup": bool(rec.get("dedup")),
-            "weights_layout": ("tiled (jet_tile_weights once, before timing)" if args.w_layout == "tiled"
+            "weights_layout": ("tiled (jet_tile_weights once, before timing)" if rec["w_layout"] == "tiled"
                                else "row-major"),
             "row_gather": (f"rows read in place from a right-padded [N, {rec['gather_rows']}, d] source "
                            "(one compaction launch, then the head's tiled loads)") if rec.get("gather_rows") else None,
@@ -875,7 +881,8 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default="large", choices=sorted(WORKLOADS),
                     help="the headline workload (default: the large 20k-row batch, the largest)")
     ap.add_argument("--per-config",
-                    default="binary,binary-restricted,binary-both,binary-gather,multitoken,wideschema,large-dedup",
+                    default="binary,binary-restricted,binary-both,binary-gather,multitoken,wideschema,large-dedup,"
+                            "large-rowmajor",
                     help="other workloads timed the same way into the line's per_config block ('none': skip)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--w-layout", default="tiled", choices=["rowmajor", "tiled"],
