@@ -48,15 +48,18 @@ Plan make_plan(int N, int V, int d, int G, int units_cap, bool pair) {
   return p;
 }
 
+// Diagnostic switches are read once per process; the function-local statics
+// that hold them are initialised thread-safely.  Unset: -1.
+static int env_switch(const char* name) {
+  const char* v = std::getenv(name);
+  return v ? std::atoi(v) : -1;
+}
+
 // The paired head serves every batch of more than one 128-row tile: it halves
 // each CTA's share of the W tile, which keeps twice the W bytes in flight per
 // SM.  JETSCORE_HEAD_PAIR=0/1 forces a variant (diagnostics).
 bool head_use_pair(int N) {
-  static int env = -2;
-  if (env == -2) {
-    const char* v = std::getenv("JETSCORE_HEAD_PAIR");
-    env = v ? std::atoi(v) : -1;
-  }
+  static const int env = env_switch("JETSCORE_HEAD_PAIR");
   if (env >= 0) return env != 0;
   return N > BM;
 }
@@ -64,11 +67,7 @@ bool head_use_pair(int N) {
 // Dynamic unit order for the paired head when the schedule has more than one
 // wave of units (JETSCORE_HEAD_DYN=0: fixed stride, diagnostics).
 bool head_use_dynamic(const Plan& p) {
-  static int env = -2;
-  if (env == -2) {
-    const char* v = std::getenv("JETSCORE_HEAD_DYN");
-    env = v ? std::atoi(v) : -1;
-  }
+  static const int env = env_switch("JETSCORE_HEAD_DYN");
   if (env == 0) return false;
   return p.pair && p.units > p.grid / 2;
 }
@@ -80,19 +79,14 @@ bool head_use_dynamic(const Plan& p) {
 constexpr int RESTRICTED_TC_MIN_UNION = 192;
 
 bool restricted_use_tc(int n_union, int staging_rows) {
-  static int env = -2;
-  if (env == -2) {
-    const char* v = std::getenv("JETSCORE_RESTRICTED_TC");
-    env = v ? std::atoi(v) : -1;
-  }
+  static const int env = env_switch("JETSCORE_RESTRICTED_TC");
   if (n_union > staging_rows || env == 0) return false;
   return env > 0 || n_union >= RESTRICTED_TC_MIN_UNION;
 }
 
 bool pdl_enabled() {
-  static int on = -1;
-  if (on < 0) on = std::getenv("JETSCORE_NO_PDL") ? 0 : 1;
-  return on == 1;
+  static const bool on = std::getenv("JETSCORE_NO_PDL") == nullptr;
+  return on;
 }
 
 }  // namespace jet
