@@ -7,11 +7,12 @@
 //
 // with ctr(v) = v - mean(v) and rms(v) = ||v|| / sqrt(m).  Each input's logit
 // vector (its candidate logits) is a CSR segment.
-//   d pass    one warp per (input, group of 8 layers), lanes over the
+//   d pass    one warp per (input, group of 32 layers), lanes over the
 //             segment's elements (coalesced): the input's logits stay in
 //             registers (segments up to 256 logits; longer ones take a
 //             two-pass loop over memory), the layers' segments are loaded
-//             16 values per lane at a time, and the layers' means and centred
+//             16 values per lane at a time, the next batch's loads issued
+//             before this batch is reduced, and the layers' means and centred
 //             sums of squares are reduced together (transpose_reduce, fixed
 //             order); rms(ctr(z)) is exactly
 //             0 for a flat vector; each warp validates its own segment before
@@ -44,7 +45,7 @@ __device__ __forceinline__ float wmax_s(float v) {
   return v;
 }
 
-constexpr int SENS_LG = 8;   // layers per warp in the d pass
+constexpr int SENS_LG = 32;  // layers per warp in the d pass
 
 // Sums over the warp of SB values per lane (one per layer), SB a power of two
 // <= 32, in 5 + (SB - 1) - log2(SB) shuffles instead of 5 * SB: at each of the
@@ -88,9 +89,24 @@ __device__ __forceinline__ int rt_lane(int u) {
   return l;
 }
 
+// One input's segment (elements b + lane + 32 j of each layer row, VPL per
+// lane) in SB consecutive layers from layer l, one load each; layers past the
+// last one load the last layer again (never stored).
+template <int VPL, int SB>
+__device__ __forceinline__ void sens_load_batch(const SensArgs& a, int l, int b, int lane, const bool (&in)[VPL],
+                                                float (&dv)[SB][VPL]) {
+#pragma unroll
+  for (int u = 0; u < SB; ++u) {
+    const float* zs = a.z_skip + (size_t)min(l + u, a.L - 1) * a.total;
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) dv[u][j] = in[j] ? zs[b + lane + 32 * j] : 0.f;
+  }
+}
+
 // d for layers [l0, l0 + SENS_LG) of input x, its segment [b, e) held as VPL
 // values per lane (element b + lane + 32 j); the segments of SB layers are
-// loaded together (SB * VPL = 16 loads in flight per lane).
+// loaded together (SB * VPL = 16 loads per lane), and the next SB layers'
+// loads are issued before this batch is reduced.
 template <int VPL>
 __device__ __forceinline__ void sens_d_regs(const SensArgs& a, int x, int l0, int b, int e, int lane) {
   constexpr int SB = 16 / VPL;
@@ -117,16 +133,13 @@ __device__ __forceinline__ void sens_d_regs(const SensArgs& a, int x, int l0, in
   // a flat logit vector has rms(ctr(z)) = 0 exactly (fp32 centring would leave ulps)
   const bool flat = wmin_s(lo) == wmax_s(hi);
   const float rz = flat ? SENS_EPS : fmaxf(SENS_EPS, sqrtf(wsum_s(qz) * inv_m));
+  float dv[SB][VPL];
+  sens_load_batch<VPL, SB>(a, l0, b, lane, in, dv);
 #pragma unroll 1
   for (int t0 = 0; t0 < SENS_LG; t0 += SB) {
-    float dv[SB][VPL];
-#pragma unroll
-    for (int u = 0; u < SB; ++u) {
-      const int l = min(l0 + t0 + u, a.L - 1);   // past the last layer: a duplicate load, not stored
-      const float* zs = a.z_skip + (size_t)l * a.total;
-#pragma unroll
-      for (int j = 0; j < VPL; ++j) dv[u][j] = in[j] ? zs[b + lane + 32 * j] : 0.f;
-    }
+    float nx[SB][VPL];
+    const bool more = t0 + SB < SENS_LG && l0 + t0 + SB < a.L;
+    if (more) sens_load_batch<VPL, SB>(a, l0 + t0 + SB, b, lane, in, nx);
     float part[SB];
 #pragma unroll
     for (int u = 0; u < SB; ++u) {
@@ -152,6 +165,11 @@ __device__ __forceinline__ void sens_d_regs(const SensArgs& a, int x, int l0, in
     const float rd = sqrtf(transpose_reduce<SB>(part, lane) * inv_m);
     const int l = l0 + t0 + rt_layer<SB>(lane);
     if (lane == rt_lane<SB>(rt_layer<SB>(lane)) && l < a.L) a.d[(size_t)l * a.n_inputs + x] = rd / rz;
+    if (!more) break;
+#pragma unroll
+    for (int u = 0; u < SB; ++u)
+#pragma unroll
+      for (int j = 0; j < VPL; ++j) dv[u][j] = nx[u][j];
   }
 }
 

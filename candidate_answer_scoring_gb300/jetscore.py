@@ -317,6 +317,88 @@ class JetScorer:
             raise JetError(rc, "jet_layer_sensitivity")
         return d, J, sel[:k]
 
+    def bind_dedup_rows(self, H: torch.Tensor, tok_row: torch.Tensor, H_unique: torch.Tensor,
+                        tok_row_unique: torch.Tensor, row_map: Optional[torch.Tensor] = None):
+        """dedup_rows with its checks and argument marshalling done once: returns
+        call, where call() makes only the (synchronous) jet_dedup_rows C call into
+        the given buffers and returns n_unique.  The tensors must stay alive and
+        unchanged in shape while call is used; their contents may change."""
+        dev = self.device
+        _check_dev(H, "H", dev, _BF16)
+        _check_dev(H_unique, "H_unique", dev, _BF16)
+        for name, t in (("tok_row", tok_row), ("tok_row_unique", tok_row_unique)):
+            _check_dev(t, name, dev, (torch.int32,))
+        if row_map is not None:
+            _check_dev(row_map, "row_map", dev, (torch.int32,))
+        if H_unique.shape != H.shape or tok_row_unique.numel() != tok_row.numel() or \
+                (row_map is not None and row_map.numel() != H.shape[0]):
+            raise ValueError("dedup_rows buffers do not match H and tok_row")
+        n = C.c_int(0)
+        args = (self._h, _ptr(H), H.shape[0], _ptr(tok_row), tok_row.numel(), _ptr(H_unique), _ptr(tok_row_unique),
+                _ptr(row_map), C.byref(n), _stream(dev))
+        fn = self.lib.jet_dedup_rows
+        held = (H, tok_row, H_unique, tok_row_unique, row_map)
+
+        def call():
+            rc = fn(*args)
+            if rc != JET_OK:
+                raise JetError(rc, "jet_dedup_rows")
+            return n.value
+
+        call.buffers = held   # the marshalled pointers stay valid while call lives
+        return call
+
+    def bind_fit_temperature(self, s, tok_ids, cand_offsets, set_offsets, gold, T_min: float = 0.05,
+                             T_max: float = 100.0):
+        """fit_temperature marshalled once: returns call, where call() makes only
+        the (synchronous) jet_fit_temperature C call and returns (T, nll)."""
+        dev = self.device
+        _check_dev(s, "s", dev, (torch.float32,))
+        for name, t in (("tok_ids", tok_ids), ("cand_offsets", cand_offsets), ("set_offsets", set_offsets),
+                        ("gold", gold)):
+            _check_dev(t, name, dev, (torch.int32,))
+        T, nll = C.c_double(0), C.c_double(0)
+        args = (self._h, _ptr(s), _ptr(tok_ids), tok_ids.numel(), _ptr(cand_offsets), cand_offsets.numel() - 1,
+                _ptr(set_offsets), set_offsets.numel() - 1, _ptr(gold), float(T_min), float(T_max), C.byref(T),
+                C.byref(nll), _stream(dev))
+        fn = self.lib.jet_fit_temperature
+        held = (s, tok_ids, cand_offsets, set_offsets, gold)
+
+        def call():
+            rc = fn(*args)
+            if rc != JET_OK:
+                raise JetError(rc, "jet_fit_temperature")
+            return T.value, nll.value
+
+        call.buffers = held
+        return call
+
+    def bind_layer_sensitivity(self, z, z_skip, offsets, k: int, d: torch.Tensor, J: torch.Tensor,
+                               selected: torch.Tensor):
+        """layer_sensitivity marshalled once, writing into d [L, n], J [L] and
+        selected [k]: returns call, where call() makes only the (synchronous)
+        jet_layer_sensitivity C call."""
+        dev = self.device
+        for name, t in (("z", z), ("z_skip", z_skip), ("d", d), ("J", J)):
+            _check_dev(t, name, dev, (torch.float32,))
+        for name, t in (("offsets", offsets), ("selected", selected)):
+            _check_dev(t, name, dev, (torch.int32,))
+        L, n = z_skip.shape[0], offsets.numel() - 1
+        if d.numel() != L * n or J.numel() != L or selected.numel() < max(int(k), 1):
+            raise ValueError("layer_sensitivity buffers do not match z_skip, offsets and k")
+        args = (self._h, _ptr(z), _ptr(z_skip), _ptr(offsets), n, z.numel(), L, int(k), _ptr(d), _ptr(J),
+                _ptr(selected), _stream(dev))
+        fn = self.lib.jet_layer_sensitivity
+        held = (z, z_skip, offsets, d, J, selected)
+
+        def call():
+            rc = fn(*args)
+            if rc != JET_OK:
+                raise JetError(rc, "jet_layer_sensitivity")
+
+        call.buffers = held
+        return call
+
     def selftest_wait_timeout(self, limit_us: int) -> int:
         """Run the bounded-wait diagnostic; returns the status (JET_ERR_TIMEOUT expected)."""
         return self.lib.jet_selftest_wait_timeout(self._h, int(limit_us), _stream(self.device))

@@ -95,3 +95,14 @@ def test_rejects_gold_outside_its_set(jet):
     with pytest.raises(j.JetError) as e:
         gpu_fit(jet, s, tok, co, so, gold)
     assert e.value.status == -3
+
+
+def test_bound_call_matches_fit_temperature(jet):
+    """bind_fit_temperature marshals once; call() is the bare C call and
+    returns the same (T, nll) as fit_temperature, bit for bit, on every call."""
+    s, tok, co, so, gold = labelled_sets(60, 1.7, seed=41)
+    sc = jet.JetScorer(64, 100, 4, max(4, tok.size))
+    args = (dev(s), dev(tok), dev(co), dev(so), dev(gold))
+    ref = sc.fit_temperature(*args)
+    call = sc.bind_fit_temperature(*args)
+    assert call() == ref and call() == ref

@@ -131,3 +131,28 @@ def test_dedup_without_tokens(jet):
     np.testing.assert_array_equal(Hu.view(torch.int16).cpu().numpy().view(np.uint16), wl.H[order])
     np.testing.assert_array_equal(row_map.cpu().numpy(), rep)
     assert tok_u.numel() == 0
+
+
+def test_bound_call_matches_dedup_rows(jet):
+    """bind_dedup_rows marshals once; each call() is the bare C call: the same
+    count and bit-identical rows and remapped token rows as dedup_rows, new
+    contents written into H are deduplicated, and a bad token row raises."""
+    wl = wk.custom(128, 900, 40, K=(2, 8), length=(1, 6), dup_prob=0.3, seed=33)
+    sc = jet.JetScorer(wl.d, wl.V, wl.N, wl.n_tok)
+    H = dev(wl.H.view(np.int16)).view(torch.bfloat16)
+    tok_row = dev(wl.tok_row)
+    Hu_ref, tok_ref, map_ref = sc.dedup_rows(H, tok_row, want_row_map=True)
+    Hu, tok_u, row_map = torch.empty_like(H), torch.empty_like(tok_row), torch.empty(wl.N, dtype=torch.int32,
+                                                                                       device="cuda")
+    call = sc.bind_dedup_rows(H, tok_row, Hu, tok_u, row_map)
+    for _ in range(2):
+        n = call()
+        assert n == Hu_ref.shape[0]
+        assert torch.equal(Hu[:n].view(torch.int16), Hu_ref.view(torch.int16))
+        assert torch.equal(tok_u, tok_ref) and torch.equal(row_map, map_ref)
+    H.copy_(H[torch.zeros(wl.N, dtype=torch.long, device="cuda")])     # every row now equals row 0
+    assert call() == 1 and torch.all(tok_u == 0)
+    tok_row[0] = wl.N
+    with pytest.raises(jet.JetError) as e:
+        call()
+    assert e.value.status == jet.JET_ERR_TOKEN_RANGE

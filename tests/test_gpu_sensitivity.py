@@ -66,3 +66,18 @@ def test_rejects_empty_input(scorer):
     with pytest.raises(jet.JetError) as e:
         scorer.layer_sensitivity(dev(z), dev(z_skip), dev(bad), 2)
     assert e.value.status == -3
+
+
+def test_bound_call_matches_layer_sensitivity(scorer):
+    """bind_layer_sensitivity marshals once into caller buffers; call() is the
+    bare C call: bit-identical d, J and selection to layer_sensitivity."""
+    z, z_skip, offsets = case(5, n=64, L=40)
+    a = (dev(z), dev(z_skip), dev(offsets))
+    d_ref, J_ref, sel_ref = scorer.layer_sensitivity(*a, 7)
+    d = torch.empty_like(d_ref)
+    J = torch.empty_like(J_ref)
+    sel = torch.empty(7, dtype=torch.int32, device="cuda")
+    call = scorer.bind_layer_sensitivity(*a, 7, d, J, sel)
+    for _ in range(2):
+        call()
+        assert torch.equal(d, d_ref) and torch.equal(J, J_ref) and torch.equal(sel, sel_ref)
