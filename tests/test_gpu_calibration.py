@@ -106,3 +106,33 @@ def test_bound_call_matches_fit_temperature(jet):
     ref = sc.fit_temperature(*args)
     call = sc.bind_fit_temperature(*args)
     assert call() == ref and call() == ref
+
+
+def test_problem_too_large_for_shared_memory():
+    """1500 sets of 20-40 candidates (about 45k): the scores, flags and
+    per-set maxima no longer fit in shared memory, so every Newton step reads
+    them from global memory; the fit still matches the oracle."""
+    import candidate_answer_scoring_gb300 as jet
+    n_sets = 1500
+    rng = np.random.default_rng(52)
+    K = rng.integers(20, 41, size=n_sets)
+    so = np.concatenate([[0], np.cumsum(K)]).astype(np.int32)
+    n_cand = int(so[-1])
+    assert n_cand * 5 + n_sets * 8 > 200 * 1024
+    tok = np.empty(n_cand, np.int32)
+    for k in range(n_sets):
+        ids = rng.choice(1000, size=K[k], replace=False)
+        if rng.random() < 0.2:
+            ids[-1] = ids[0]                        # a duplicate text: its gold class has two labels
+        tok[so[k]:so[k + 1]] = ids
+    co = np.arange(n_cand + 1, dtype=np.int32)       # one token per candidate
+    s = (rng.normal(size=n_cand) * 3).astype(np.float32)
+    for k in range(n_sets):                         # equal texts carry equal scores
+        c0, c1 = so[k], so[k + 1]
+        s[c0:c1][tok[c0:c1] == tok[c0]] = s[c0]
+    gold = np.empty(n_sets, np.int32)
+    for k in range(n_sets):
+        a = s[so[k]:so[k + 1]].astype(np.float64) / 1.6
+        p = np.exp(a - a.max()); p /= p.sum()
+        gold[k] = rng.choice(K[k], p=p)
+    check(jet, s, tok, co, so, gold)
