@@ -108,17 +108,16 @@ def test_bound_call_matches_fit_temperature(jet):
     assert call() == ref and call() == ref
 
 
-def test_problem_too_large_for_shared_memory():
-    """1500 sets of 20-40 candidates (about 45k): the scores, flags and
-    per-set maxima no longer fit in shared memory, so every Newton step reads
-    them from global memory; the fit still matches the oracle."""
+def test_large_problem():
+    """1500 sets of 20-40 candidates (about 45k, some sets with a repeated
+    text in the gold class): each of the CTA's threads takes one or two sets
+    per Newton step; the fit matches the oracle."""
     import candidate_answer_scoring_gb300 as jet
     n_sets = 1500
     rng = np.random.default_rng(52)
     K = rng.integers(20, 41, size=n_sets)
     so = np.concatenate([[0], np.cumsum(K)]).astype(np.int32)
     n_cand = int(so[-1])
-    assert n_cand * 5 + n_sets * 8 > 200 * 1024
     tok = np.empty(n_cand, np.int32)
     for k in range(n_sets):
         ids = rng.choice(1000, size=K[k], replace=False)
